@@ -1,0 +1,580 @@
+"""Throughput of the fused add + Gemma RMSNorm + quant op on GB300.
+
+One step = one call of the op over one batch of the decode workload (M=256,
+H=4096, bf16, static FP8 with y and in-place residual); the per-workload
+table adds the prefill and tensor-parallel-partial shapes.  Prints ONE JSON
+line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gnq|reference]
+
+Timing: W untimed steps, then exactly K steps captured in one CUDA graph and
+timed with CUDA events on the capture stream, bracketed by a barrier and a
+device synchronize.  Every step reads a different input set; the sets
+together exceed twice the L2 size, so no step finds its inputs in L2.  Under
+torchrun every rank runs an independent replica (rows are independent, there
+is no data exchange); the slowest rank's time is reported and the value is
+the bytes all ranks moved over that time.
+
+--impl reference times the CPU oracle (the plain C restatement of the method)
+on the same workload, metric and unit, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from nvfp4_quant_gemma_gb300.workloads import HEADLINE, WORKLOADS, DTYPES, make_inputs  # noqa: E402
+
+METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s for add+GemmaRMSNorm+quant"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["nvfp4_quant_gemma_gb300/csrc/gnq_kernels.cuh",
+                  "nvfp4_quant_gemma_gb300/csrc/gnq_launch.cuh",
+                  "nvfp4_quant_gemma_gb300/csrc/gnq_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    try:
+        lines = open(TRAFFIC_FILE).read().splitlines()
+    except OSError:
+        return None
+    src_hash = None
+    table = {}
+    for ln in lines:
+        ln = ln.strip()
+        if not ln or ln.startswith("#"):
+            continue
+        parts = ln.split()
+        if parts[0] == "kernel_sources_sha256_16":
+            src_hash = parts[1]
+        elif len(parts) >= 2:
+            table[parts[0]] = parts[1]
+    if src_hash != kernel_hash() or workload not in table:
+        return None
+    v = table[workload]
+    return None if v == "null" else float(v)
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons over a window."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 10:
+                continue
+            if self.uuid and f[1] != self.uuid:
+                continue
+            rows.append(f)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        smax = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        power = [float(r[4]) for r in rows if r[4].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+def device_uuid(dev: torch.device):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+def _device_inputs(wl, dev, exact: bool):
+    """Inputs on the device: the seeded CPU recipe (exact), or the same
+    distributions drawn with a seeded device generator (fast, for big shapes)."""
+    if exact:
+        return make_inputs(wl, dev)
+    g = torch.Generator(device=dev).manual_seed(wl.seed)
+    T = DTYPES[wl.dtype]
+    M, H = wl.M, wl.H
+    out = {}
+    if wl.k > 1:
+        out["x"] = (torch.randn(wl.k, M, H, generator=g, device=dev) * math.sqrt(wl.part_var)).to(T)
+    else:
+        out["x"] = (torch.randn(M, H, generator=g, device=dev) * math.sqrt(wl.x_var)).to(T)
+    if wl.residual:
+        r = torch.randn(M, H, generator=g, device=dev) * math.sqrt(wl.r_var)
+        if wl.n_outliers:
+            from nvfp4_quant_gemma_gb300.workloads import outlier_channels
+            r[:, outlier_channels(wl).to(dev)] *= wl.outlier_mult
+        out["residual"] = r.to(T)
+    else:
+        out["residual"] = None
+    out["weight"] = (torch.randn(H, generator=g, device=dev) * math.sqrt(wl.w_var)).to(T)
+    out["scale"] = torch.tensor([wl.scale], dtype=torch.float32, device=dev)
+    out["eps"] = wl.eps
+    return out
+
+
+class Case:
+    """Rotating input/output sets of one workload and the call that runs a step."""
+
+    def __init__(self, gnq, wl, dev, exact_inputs: bool, l2_bytes: int):
+        self.gnq, self.wl, self.dev = gnq, wl, dev
+        base = _device_inputs(wl, dev, exact_inputs)
+        self.w, self.scale, self.eps = base["weight"], base["scale"], base["eps"]
+        per_set = wl.algorithmic_bytes()
+        free = torch.cuda.mem_get_info(dev)[0]
+        self.n_sets = max(2, min(64, math.ceil(2.5 * l2_bytes / per_set)))
+        self.n_sets = max(1, min(self.n_sets, int(0.5 * free // max(1, 2 * per_set))))
+        self.sets = []
+        for i in range(self.n_sets):
+            x = base["x"] if i == 0 else base["x"].clone()
+            r = None if base["residual"] is None else (base["residual"] if i == 0 else base["residual"].clone())
+            out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, wl.write_y, x)
+            self.sets.append((x, r, out))
+        self.footprint = per_set * self.n_sets
+
+    def step(self, i: int, stream=None):
+        x, r, out = self.sets[i % self.n_sets]
+        wl = self.wl
+        if wl.k > 1:
+            self.gnq.gemma_add_rms_norm_quant_parts(x, r, self.w, self.eps, self.scale, wl.mode,
+                                                    write_y=wl.write_y, out=out, stream=stream)
+        elif wl.mode == "none":
+            self.gnq.gemma_add_rms_norm(x, r, self.w, self.eps, y=out[2], stream=stream)
+        else:
+            self.gnq.gemma_add_rms_norm_quant(x, r, self.w, self.eps, self.scale, wl.mode,
+                                              write_y=wl.write_y, out=out, stream=stream)
+
+    def graph(self, n: int, start: int = 0):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(self.dev)
+        s.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(s):
+            self.step(0)  # first launch outside capture (library init)
+        torch.cuda.current_stream(self.dev).wait_stream(s)
+        torch.cuda.synchronize(self.dev)
+        with torch.cuda.graph(g):
+            for i in range(n):
+                self.step(start + i)
+        return g
+
+
+def time_graph(g, dev, n_steps: int, barrier=None, soak_s: float = 0.0, sampler=None):
+    """Replay g once inside CUDA events (after optional soak replays)."""
+    stream = torch.cuda.current_stream(dev)
+    ctx = sampler if sampler is not None else _Null()
+    with ctx:
+        t_end = time.time() + soak_s
+        while time.time() < t_end:
+            g.replay()
+            torch.cuda.synchronize(dev)
+        if barrier:
+            barrier()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if barrier:
+            barrier()
+        ms = e0.elapsed_time(e1)
+        t_end = time.time() + soak_s
+        while time.time() < t_end:
+            g.replay()
+            torch.cuda.synchronize(dev)
+    return ms
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        pass
+
+
+def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory, runs the op, and reads its results
+    back into pinned host memory."""
+    inp = make_inputs(wl)
+    n_host = 4
+    host_in = []
+    for i in range(n_host):
+        x = inp["x"].clone().pin_memory()
+        r = None if inp["residual"] is None else inp["residual"].clone().pin_memory()
+        host_in.append((x, r))
+    xd = torch.empty_like(inp["x"], device=dev)
+    rd = None if inp["residual"] is None else torch.empty_like(inp["residual"], device=dev)
+    w = inp["weight"].to(dev)
+    s = inp["scale"].to(dev)
+    out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, wl.write_y, xd)
+    host_out = [None if t is None else torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for t in out]
+    host_r = None if rd is None else torch.empty(rd.shape, dtype=rd.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_in[0] if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in host_out if t is not None)
+    d2h += 0 if host_r is None else host_r.numel() * host_r.element_size()
+
+    def one(i):
+        hx, hr = host_in[i % n_host]
+        xd.copy_(hx, non_blocking=True)
+        if rd is not None:
+            rd.copy_(hr, non_blocking=True)
+        if wl.k > 1:
+            gnq.gemma_add_rms_norm_quant_parts(xd, rd, w, wl.eps, s, wl.mode, write_y=wl.write_y, out=out)
+        else:
+            gnq.gemma_add_rms_norm_quant(xd, rd, w, wl.eps, s, wl.mode, write_y=wl.write_y, out=out)
+        for h, d in zip(host_out, out):
+            if h is not None:
+                h.copy_(d, non_blocking=True)
+        if rd is not None:
+            host_r.copy_(rd, non_blocking=True)
+
+    for i in range(warmup):
+        one(i)
+    torch.cuda.synchronize(dev)
+    if barrier:
+        barrier()
+    stream = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        one(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1)
+    return ms, h2d, d2h
+
+
+def cpu_baseline(wl, budget_s: float = 10.0):
+    """The oracle as it stands, on the host cores, over repeated passes of a
+    row sample of the workload for about budget_s seconds."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    rows = min(wl.M, 256)
+    sample = wl.with_rows(rows)
+    inp = make_inputs(sample)
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    x = bits(inp["x"])
+    r = None if inp["residual"] is None else bits(inp["residual"])
+    w = bits(inp["weight"])
+    mode = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4, "mxfp8": oracle.MODE_MXFP8,
+            "none": oracle.MODE_NONE}[wl.mode]
+    dc = 0 if wl.dtype == "bf16" else 1
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = sample.algorithmic_bytes() * passes / el / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{passes} passes over {rows} rows of {wl.name} ({el:.1f} s)",
+            "tokens_per_s": rows * passes / el}
+
+
+def run_gnq(args, rank: int, world: int, barrier):
+    import nvfp4_quant_gemma_gb300 as gnq
+    from nvfp4_quant_gemma_gb300 import build as libbuild
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    if libbuild.is_stale():
+        libbuild.build()
+    gnq.load()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    peak, peak_kind = measured_peak()
+
+    wl = WORKLOADS[args.workload]
+    case = Case(gnq, wl, dev, exact_inputs=True, l2_bytes=l2)
+    g_warm = case.graph(max(args.warmup, 1))
+    g_timed = case.graph(args.steps, start=args.warmup)
+    g_warm.replay()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None
+    ms = time_graph(g_timed, dev, args.steps, barrier=barrier, soak_s=args.soak, sampler=sampler)
+    ms_t = torch.tensor([ms], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        ms_t = ms_t.to(dev) if dist.get_backend() == "nccl" else ms_t
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    bytes_step = wl.algorithmic_bytes()
+    value = bytes_step * args.steps * world / (ms_max / 1e3) / 1e9
+    per_launch_s = ms / 1e3 / args.steps
+    achieved = bytes_step / per_launch_s / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        # end to end through the public API with host buffers
+        e2e_steps = max(1, min(args.steps, 500, int(4e9 // bytes_step)))
+        e2e_ms, h2d, d2h = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier)
+        e2e_t = torch.tensor([e2e_ms], dtype=torch.float64)
+        if world > 1:
+            import torch.distributed as dist
+            e2e_t = e2e_t.to(dev) if dist.get_backend() == "nccl" else e2e_t
+            dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+        e2e_value = bytes_step * e2e_steps * world / (float(e2e_t.item()) / 1e3) / 1e9
+        e2e = {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "how": "pinned host inputs copied in, op via the Python API, results copied out"}
+
+    if rank != 0:
+        return None
+    traffic = recorded_traffic(wl.name)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded normals; no dataset or weights involved)",
+        "config": {
+            "workload": wl.name, "M": wl.M, "H": wl.H, "io_dtype": wl.dtype, "mode": wl.mode,
+            "write_y": wl.write_y, "residual": wl.residual, "partials": wl.k,
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": f"{case.n_sets} rotating input/output sets, {case.footprint / 1e6:.0f} MB "
+                  f"> 2x L2 ({l2 / 1e6:.0f} MB)",
+            "tokens_per_s": wl.M * args.steps * world / (ms_max / 1e3),
+            "us_per_call": ms_max / args.steps * 1e3,
+            "pct_of_peak": round(100 * achieved / peak, 1),
+            "timing": "K launches captured in one CUDA graph, CUDA events on the capture stream",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "peak_kind": peak_kind,
+            "algorithmic_bytes_per_launch": bytes_step,
+            "kernel": "gnq::row_kernel",
+        },
+        "gpu_launches": args.steps,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    line["clocks"] = sampler.summary() if sampler else None
+    if world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
+    if world == 1 and not args.no_table:
+        line["workloads"] = workload_table(gnq, dev, l2, peak)
+    return line
+
+
+def workload_table(gnq, dev, l2, peak):
+    rows = []
+    for name, wl in WORKLOADS.items():
+        case = Case(gnq, wl, dev, exact_inputs=(wl.M * wl.H <= 2 ** 22), l2_bytes=l2)
+        probe = case.graph(max(2, case.n_sets))
+        probe.replay()
+        torch.cuda.synchronize(dev)
+        t = time_graph(probe, dev, case.n_sets) / case.n_sets
+        n = int(min(4000, max(20, 0.3e3 / max(t, 1e-4))))
+        g = case.graph(n)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ms = time_graph(g, dev, n)
+        per = ms / n
+        b = wl.algorithmic_bytes()
+        gbs = b / (per / 1e3) / 1e9
+        rows.append({"workload": name, "us_per_call": round(per * 1e3, 3), "GB_s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(wl.M / (per / 1e3)),
+                     "bytes_per_call": b, "launches_timed": n, "sets": case.n_sets,
+                     "dram_traffic_per_launch": recorded_traffic(name)})
+        del case, probe, g
+        torch.cuda.empty_cache()
+    return rows
+
+
+# ----------------------------------------------------------------------------
+# the reference arm: the CPU oracle
+# ----------------------------------------------------------------------------
+
+def run_reference(args, rank: int):
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    wl = WORKLOADS[args.workload]
+    bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    mode = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4, "mxfp8": oracle.MODE_MXFP8,
+            "none": oracle.MODE_NONE}[wl.mode]
+    dc = 0 if wl.dtype == "bf16" else 1
+    # size one step so the K steps take about args.ref_budget seconds
+    probe = wl.with_rows(min(wl.M, 16))
+    pin = make_inputs(probe)
+    t0 = time.perf_counter()
+    oracle.gemma_add_rms_norm_quant(bits(pin["x"]), None if pin["residual"] is None else bits(pin["residual"]),
+                                    bits(pin["weight"]), wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+    per_row = (time.perf_counter() - t0) / probe.M
+    rows = int(max(1, min(wl.M, args.ref_budget / max(1, args.steps) / max(per_row, 1e-9))))
+    sample = wl.with_rows(rows)
+    inp = make_inputs(sample)
+    x = bits(inp["x"])
+    r = None if inp["residual"] is None else bits(inp["residual"])
+    w = bits(inp["weight"])
+    for _ in range(args.warmup):
+        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+    el = time.perf_counter() - t0
+    value = sample.algorithmic_bytes() * args.steps / el / 1e9
+    sample_txt = f"{rows} of {wl.M} rows of {wl.name} per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals)",
+        "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "io_dtype": wl.dtype,
+                   "mode": wl.mode, "sample": sample_txt},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample_txt},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ----------------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gnq", choices=["gnq", "reference"])
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--soak", type=float, default=0.6,
+                    help="seconds of identical replays before and after the timed replay, "
+                         "so the clock sampler sees the load")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-table", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone runs it; other ranks exit without work
+        line = run_reference(args, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist.init_process_group(backend)
+        barrier = dist.barrier
+
+    line = run_gnq(args, rank, world, barrier)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

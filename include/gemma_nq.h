@@ -1,0 +1,183 @@
+/*
+ * gemma_nq -- fused residual add + Gemma RMSNorm + next-linear input
+ * quantization on one GB300 (sm_103a), as a C ABI.
+ *
+ * The operation ("vllm.models.qwen3_5.nvidia.ops.fused_norm_quant", module
+ * docstring and gemma_add_rms_norm_quant):
+ *
+ *     h  = x + residual                 (rounded to the activation dtype;
+ *                                        written back into `residual`)
+ *     y  = dtype(h * rsqrt(mean(h^2) + eps) * (1 + w))
+ *     q  = quant(y)                     (computed from the rounded y)
+ *
+ * with quant one of
+ *   GNQ_FP8   static per-tensor FP8 E4M3: q = e4m3_satfinite(y / scale);
+ *   GNQ_NVFP4 per 16-element block: E4M3 block scale
+ *             sf = e4m3_satfinite(g * (amax / 6)), codes
+ *             e2m1_satfinite(y * (g / sf)) packed two per byte, the
+ *             lower-indexed element in the low nibble; block scales in the
+ *             128x4 swizzled layout of shape (round_up(M,128),
+ *             round_up(H/16,4)), byte (m, b) at
+ *             ((m/128)*(Kp/4) + b/4)*512 + (m%32)*16 + ((m%128)/32)*4 + b%4;
+ *   GNQ_MXFP8 per 32-element block ("vllm.model_executor.layers.
+ *             fused_allreduce_gemma_rms_norm", allreduce_gemma_rms_norm_mxfp8):
+ *             E8M0 scale code floor(log2(amax)) - 8 + 127 clamped to
+ *             [0, 254] (0 for an all-zero block), stored row-major (M, H/32);
+ *             codes e4m3_satfinite(y / 2^(code - 127)).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers on the current CUDA device, in
+ *    row-major contiguous layout.  Activations x, residual, y and the weight
+ *    w are 16-bit, of the type named by `dtype` (GNQ_BF16 or GNQ_FP16).
+ *  - The caller owns and allocates every buffer.  The library allocates
+ *    nothing per call and keeps no state other than cached device properties.
+ *  - x, w, scale and the partial buffers are read only.  `residual` (when not
+ *    NULL) is updated in place to the rounded x + residual.  q, block_scale
+ *    and y are written.  Rows m >= M of the NVFP4 scale tensor are NOT
+ *    written (their bytes keep whatever the caller put there).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream).  Nothing is synchronised and no host copy is made.
+ *  - M == 0 returns GNQ_OK without launching anything.
+ *  - Every call returns a gnq_status; the library never aborts, exits or
+ *    traps.  Argument checks happen before any launch; a rejected call has
+ *    no effect.
+ *  - Alignment: x, residual, w, y, q and every partial buffer must be 16-byte
+ *    aligned, block_scale 4-byte aligned, scale 4-byte aligned
+ *    (GNQ_ERR_ALIGN).  H must be a multiple of 8 (GNQ_ERR_SHAPE); NVFP4 needs
+ *    H % 64 == 0 (whole 4-column scale tiles, so padded scale columns never
+ *    exist) and MXFP8 H % 32 == 0.  H is at most 65536.
+ *  - x and residual must not be the same buffer, and y must differ from both
+ *    (GNQ_ERR_ALIAS).
+ */
+#ifndef GEMMA_NQ_H
+#define GEMMA_NQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GNQ_OK = 0,
+    GNQ_ERR_NULL = 1,  /* a required pointer is NULL                        */
+    GNQ_ERR_SHAPE = 2, /* M < 0, H out of range or not a supported multiple */
+    GNQ_ERR_DTYPE = 3, /* dtype is not GNQ_BF16 / GNQ_FP16                  */
+    GNQ_ERR_MODE = 4,  /* unknown quantization mode, or k out of range      */
+    GNQ_ERR_ALIAS = 5, /* x == residual, or y aliases x or residual         */
+    GNQ_ERR_ALIGN = 6, /* a pointer or the partial stride is misaligned     */
+    GNQ_ERR_CUDA = 7   /* the CUDA runtime reported an error at launch      */
+} gnq_status;
+
+typedef enum { GNQ_BF16 = 0, GNQ_FP16 = 1 } gnq_dtype;
+
+typedef enum { GNQ_FP8 = 0, GNQ_NVFP4 = 1, GNQ_MXFP8 = 2 } gnq_mode;
+
+/*
+ * Residual add + Gemma RMSNorm, no quantization
+ * ("vllm.model_executor.layers.fused_allreduce_gemma_rms_norm",
+ * fused_allreduce_gemma_rms_norm: at tensor-parallel size 1 it is
+ * norm(hidden_states, residual), returning (normed, new residual)).
+ *
+ *   x        (M, H) activation, read only.
+ *   residual (M, H) or NULL; updated in place to dtype(x + residual).
+ *   w        (H,) Gemma weight; the norm multiplies by (1 + w).
+ *   eps      RMSNorm epsilon.
+ *   y        (M, H) output, y = dtype(h * rsqrt(mean(h^2) + eps) * (1 + w)).
+ */
+int gemma_add_rms_norm(const void *x, void *residual, const void *w, float eps,
+                       void *y, int64_t M, int64_t H, int dtype, void *stream);
+
+/*
+ * Residual add + Gemma RMSNorm + the next linear's input quantization, in one
+ * pass ("vllm.models.qwen3_5.nvidia.ops.fused_norm_quant",
+ * gemma_add_rms_norm_quant).
+ *
+ *   x, residual, w, eps   as for gemma_add_rms_norm.
+ *   scale        device pointer to ONE fp32: the static FP8 scale s, or the
+ *                NVFP4 global scale g (input_global_scale_inv).  Read on the
+ *                device, so it may change between graph replays.  Unused
+ *                (may be NULL) for GNQ_MXFP8.
+ *   mode         GNQ_FP8, GNQ_NVFP4 or GNQ_MXFP8.
+ *   write_y      nonzero: also store the normed activation y (M, H).
+ *   q            FP8 / MXFP8: (M, H) E4M3 codes.  NVFP4: (M, H/2) bytes of
+ *                packed E2M1 codes.
+ *   block_scale  NVFP4: the swizzled (round_up(M,128), round_up(H/16,4))
+ *                E4M3 scale bytes.  MXFP8: (M, H/32) E8M0 codes.  Unused
+ *                (may be NULL) for GNQ_FP8, whose block scale is `scale`.
+ *   y            (M, H) if write_y, else ignored (may be NULL).
+ */
+int gemma_add_rms_norm_quant(const void *x, void *residual, const void *w,
+                             float eps, const float *scale, int mode,
+                             int write_y, void *q, void *block_scale, void *y,
+                             int64_t M, int64_t H, int dtype, void *stream);
+
+/*
+ * As gemma_add_rms_norm_quant, with the activation given as k partial
+ * buffers, the per-rank partial outputs of a row-parallel linear that a
+ * tensor-parallel all-reduce would sum ("vllm.models.qwen3_5.nvidia.ops.
+ * fused_allreduce_norm_quant", fused_allreduce_gemma_rms_norm_quant:
+ * hidden_states is the per-rank partial, reduced with fp32 accumulation).
+ * Here the k partials sit in this GPU's memory and are summed locally:
+ * a = dtype(((p0 + p1) + p2) + ...) in fp32, then h = dtype(a + residual).
+ *
+ *   x_parts      base of k (M, H) buffers; partial p starts at
+ *                x_parts + p * part_stride ELEMENTS (part_stride >= M*H and a
+ *                multiple of 8, so every partial is 16-byte aligned).
+ *   k            number of partials, 1..8 (GNQ_ERR_MODE otherwise).
+ *   mode         as above, or -1 for no quantization (then write_y must be
+ *                nonzero and q / block_scale / scale are ignored).
+ */
+int gemma_add_rms_norm_quant_parts(const void *x_parts, int k,
+                                   int64_t part_stride, void *residual,
+                                   const void *w, float eps,
+                                   const float *scale, int mode, int write_y,
+                                   void *q, void *block_scale, void *y,
+                                   int64_t M, int64_t H, int dtype,
+                                   void *stream);
+
+/*
+ * Plain (non-Gemma) RMSNorm variant: y = dtype(h * rsqrt(mean(h^2) + eps) * w),
+ * i.e. weight bias 0 instead of 1 ("vllm.models.qwen3_5.nvidia.ops.
+ * fused_allreduce_norm_quant" passes the weight bias to the fused kernel;
+ * weight_bias=1.0 marks the Gemma form on
+ * "vllm.model_executor.layers.fused_allreduce_gemma_rms_norm").  Arguments
+ * as for gemma_add_rms_norm_quant_parts; k = 1 for a single activation.
+ */
+int add_rms_norm_quant(const void *x_parts, int k, int64_t part_stride,
+                       void *residual, const void *w, float eps,
+                       const float *scale, int mode, int write_y, void *q,
+                       void *block_scale, void *y, int64_t M, int64_t H,
+                       int dtype, void *stream);
+
+/* Human-readable text of a gnq_status (static storage, never NULL). */
+const char *gnq_status_string(int status);
+
+/*
+ * Tuning hook: force the launch shape of later calls in this process --
+ * `cluster` CTAs per row (0 = automatic, else 1, 2, 4 or 8) and `vpt`
+ * 16-byte chunks per thread (0 = automatic, else 1, 2 or 4).  A forced shape
+ * that does not fit a call's H and mode is ignored for that call.  The shape
+ * only changes the order in which a row's squares are summed (so y may move
+ * by one rounding step); the residual, and the codes of a given y, do not
+ * depend on it.  Not synchronised with calls in flight on other host
+ * threads.  Returns GNQ_ERR_SHAPE for values outside those sets.
+ */
+int gnq_set_launch_policy(int cluster, int vpt);
+
+/*
+ * Diagnostic: the element encoders the kernels use, applied to n fp32 values
+ * v (device pointer): e4m3[i] = the E4M3 satfinite round-to-nearest-even code
+ * of v[i], e2m1[i] = the E2M1 satfinite round-to-nearest-even code (low
+ * nibble).  Either output may be NULL.  Lets a test compare the hardware
+ * conversions with an independent encoder on special values (ties, zero
+ * signs, subnormals, saturation).
+ */
+int gnq_encode_e4m3_e2m1(const float *v, int64_t n, uint8_t *e4m3,
+                         uint8_t *e2m1, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GEMMA_NQ_H */

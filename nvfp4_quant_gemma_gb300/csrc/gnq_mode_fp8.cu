@@ -1,0 +1,7 @@
+// Instances of the row kernel for quantization mode FP8.
+#include "gnq_launch.cuh"
+
+namespace gnq {
+template cudaError_t launch_mode<MODE_FP8>(const Params &, int, bool, const LaunchShape &,
+                                            cudaStream_t);
+}  // namespace gnq

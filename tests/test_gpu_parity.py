@@ -1,0 +1,325 @@
+"""GPU parity: the sm_103a library against the CPU oracle, through the C ABI.
+
+Rules (the method's correctness contract):
+  * the updated residual is bit-exact;
+  * y is within 1 unit in the last place of the activation dtype (relative
+    2^-8 for bf16, 2^-11 for fp16) of the oracle's fp64 norm;
+  * codes and block scales are bit-exact when the oracle quantizes the GPU's
+    own y (the same fp32 decisions on both sides);
+  * end to end (oracle y -> oracle codes vs GPU codes) at most 1e-4 of the
+    elements differ, each by at most one adjacent code;
+  * NVFP4 scale rows >= M, and bytes around every output, are untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gnq_testutil import (DTYPE_CODE, DTYPES, bits, e2m1_signed_rank, e4m3_signed_rank, u8,
+                          ulp_distance16, unpack_nibbles)
+
+pytestmark = pytest.mark.gpu
+
+OMODE = {"none": oracle.MODE_NONE, "fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4,
+         "mxfp8": oracle.MODE_MXFP8}
+SENT = 0xA5
+GUARD = 256
+
+
+@pytest.fixture(scope="module")
+def gnq():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from nvfp4_quant_gemma_gb300 import build
+    build.build()
+    import nvfp4_quant_gemma_gb300 as pkg
+    pkg.load()
+    pkg.set_launch_policy(0, 0)
+    oracle.build()
+    import os
+    oracle.set_threads(os.cpu_count() or 1)
+    return pkg
+
+
+def _guarded(shape, dtype, dev):
+    """A tensor inside a sentinel-filled buffer with GUARD bytes on each side."""
+    nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+    buf = torch.full((nbytes + 2 * GUARD,), SENT, dtype=torch.uint8, device=dev)
+    t = buf[GUARD:GUARD + nbytes].view(dtype).view(shape)
+    return buf, t
+
+
+def _guards_intact(buf):
+    b = buf.cpu().numpy()
+    return bool(np.all(b[:GUARD] == SENT) and np.all(b[-GUARD:] == SENT))
+
+
+def _make(M, H, dtype, seed, k=1, residual=True, r_std=3.0, w_std=0.3, special=True):
+    g = torch.Generator().manual_seed(seed)
+    T = DTYPES[dtype]
+    x = torch.randn((k, M, H) if k > 1 else (M, H), generator=g)
+    if k > 1:
+        x = x * 0.5
+    r = torch.randn(M, H, generator=g) * r_std if residual else None
+    w = torch.randn(H, generator=g) * w_std
+    if special and M >= 3 and residual:
+        r[:, :: max(1, H // 7)] *= 20.0  # outlier channels (saturate FP8/NVFP4)
+        r[1] = 0.0                       # row 1: residual zero
+        x[..., 2, :] = 0.0               # row 2: x zero
+        if M >= 4:
+            r[3] = 0.0
+            x[..., 3, :] = 0.0           # row 3: all zero -> y = 0, scales 0
+    return x.to(T), (None if r is None else r.to(T)), w.to(T)
+
+
+def run_case(gnq, x, r, w, mode, scale, write_y, dtype, eps=1e-6, weight_bias=1.0, check_e2e=True):
+    """Run GPU and oracle on the same inputs and assert every parity rule."""
+    dev = torch.device("cuda")
+    T = DTYPES[dtype]
+    dc = DTYPE_CODE[dtype]
+    k = x.shape[0] if x.dim() == 3 else 1
+    M, H = x.shape[-2:]
+    om = OMODE[mode]
+    ref = oracle.gemma_add_rms_norm_quant(bits(x), None if r is None else bits(r), bits(w), eps,
+                                          scale, om, dc, write_y=True, weight_bias=weight_bias)
+
+    xd, wd = x.to(dev), w.to(dev)
+    sd = torch.tensor([scale], dtype=torch.float32, device=dev)
+    results = {}
+    for wy in sorted({True, bool(write_y)}):
+        rd_buf, rd = (None, None) if r is None else _guarded((M, H), T, dev)
+        if rd is not None:
+            rd.copy_(r.to(dev))
+        qb = bsb = yb = None
+        q = bs = y = None
+        if om in (oracle.MODE_FP8, oracle.MODE_MXFP8):
+            qb, q = _guarded((M, H), torch.uint8, dev)
+        elif om == oracle.MODE_NVFP4:
+            qb, q = _guarded((M, H // 2), torch.uint8, dev)
+        if om == oracle.MODE_NVFP4:
+            bsb, bs = _guarded(oracle.scale_shape(M, H, om), torch.uint8, dev)
+        elif om == oracle.MODE_MXFP8:
+            bsb, bs = _guarded(oracle.scale_shape(M, H, om), torch.uint8, dev)
+        if wy or om == oracle.MODE_NONE:
+            yb, y = _guarded((M, H), T, dev)
+        if k == 1 and weight_bias == 1.0:
+            if om == oracle.MODE_NONE:
+                gnq.gemma_add_rms_norm(xd, rd, wd, eps, y=y)
+            else:
+                gnq.gemma_add_rms_norm_quant(xd, rd, wd, eps, sd, mode, write_y=wy, out=(q, bs, y))
+        else:
+            fn = gnq.gemma_add_rms_norm_quant_parts if weight_bias == 1.0 else gnq.add_rms_norm_quant
+            fn(xd, rd, wd, eps, sd, mode, write_y=wy, out=(q, bs, y))
+        torch.cuda.synchronize()
+        for b in (rd_buf, qb, bsb, yb):
+            if b is not None:
+                assert _guards_intact(b), "a write landed outside its buffer"
+        results[wy] = dict(r=rd, q=q, bs=bs, y=y)
+
+    full = results[True]
+    # residual: bit-exact
+    if r is not None:
+        assert np.array_equal(bits(full["r"]), ref["residual"])
+    # y: within one ulp of the fp64 oracle
+    gy = bits(full["y"])
+    assert int(ulp_distance16(gy, ref["y"]).max()) <= 1
+    if om == oracle.MODE_NONE:
+        return
+    # write_y does not change the codes
+    if not write_y:
+        assert np.array_equal(u8(results[False]["q"]), u8(full["q"]))
+        if full["bs"] is not None:
+            assert np.array_equal(u8(results[False]["bs"]), u8(full["bs"]))
+        if r is not None:
+            assert np.array_equal(bits(results[False]["r"]), ref["residual"])
+    # codes from the GPU's own y: bit-exact
+    qo, bso = oracle.quantize_from_y(gy, scale, om, dc)
+    gq = u8(full["q"])
+    assert np.array_equal(gq, qo)
+    if om == oracle.MODE_NVFP4:
+        gbs = u8(full["bs"]).reshape(-1)
+        Kp = oracle.round_up(H // 16, 4)
+        written = np.zeros(gbs.size, bool)
+        for m in range(M):
+            for b in range(H // 16):
+                written[oracle.swizzle_offset(m, b, Kp)] = True
+        assert np.array_equal(gbs[written], bso.reshape(-1)[written])
+        assert np.all(gbs[~written] == SENT), "padding rows of the scale tensor were written"
+    elif om == oracle.MODE_MXFP8:
+        assert np.array_equal(u8(full["bs"]), bso)
+    # end to end: oracle codes vs GPU codes
+    if check_e2e:
+        if om == oracle.MODE_NVFP4:
+            a, b = e2m1_signed_rank(unpack_nibbles(gq)), e2m1_signed_rank(unpack_nibbles(ref["q"]))
+        else:
+            a, b = e4m3_signed_rank(gq), e4m3_signed_rank(ref["q"])
+        diff = np.abs(a - b)
+        assert int(diff.max(initial=0)) <= 1
+        assert np.count_nonzero(diff) <= max(1, int(1e-4 * diff.size))
+
+
+# --- hardware encoders vs the oracle's reading ----------------------------------
+
+def test_hardware_encoders_match_oracle(gnq):
+    rng = np.random.default_rng(0)
+    e4_vals = np.array([oracle.e4m3_value(c) for c in range(0x7F)])
+    mids = (e4_vals[:-1] + e4_vals[1:]) / 2
+    e2_vals = np.array([0, 0.5, 1, 1.5, 2, 3, 4, 6.0])
+    mids2 = (e2_vals[:-1] + e2_vals[1:]) / 2
+    v = np.concatenate([
+        rng.standard_normal(100000) * np.ldexp(1.0, rng.integers(-14, 10, 100000)),
+        mids, -mids, np.nextafter(mids.astype(np.float32), np.float32(0)),
+        np.nextafter(mids.astype(np.float32), np.float32(1e9)),
+        mids2, -mids2, e4_vals, -e4_vals,
+        [0.0, -0.0, 1e-30, -1e-30, 2.0 ** -10, 3 * 2.0 ** -11, 448.0, 464.0, 500.0, 1e30,
+         -1e30, 6.0, 6.5, 7.0, -100.0, np.inf, -np.inf, 1e-45, -1e-45]]).astype(np.float32)
+    vd = torch.from_numpy(v).cuda()
+    e4, e2 = gnq.encode_e4m3_e2m1(vd)
+    torch.cuda.synchronize()
+    v64 = v.astype(np.float64)
+    assert np.array_equal(e4.cpu().numpy(), oracle.e4m3_encode(v64))
+    assert np.array_equal(e2.cpu().numpy(), oracle.e2m1_encode(v64))
+
+
+# --- small shapes: several tiles, ragged tails, every mode ---------------------
+
+SMALL_M = [1, 3, 127, 129, 300]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0), ("mxfp8", 0.0)])
+@pytest.mark.parametrize("M", SMALL_M)
+@pytest.mark.parametrize("H", [64, 2048, 5120])
+def test_small_shapes(gnq, dtype, mode, scale, M, H):
+    x, r, w = _make(M, H, dtype, seed=M * 7 + H)
+    run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 1), dtype=dtype, check_e2e=(M * H >= 1e5))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.08), ("nvfp4", 84.0)])
+def test_no_residual(gnq, dtype, mode, scale):
+    x, _, w = _make(200, 8192, dtype, seed=11, residual=False)
+    run_case(gnq, x, None, w, mode, scale, write_y=False, dtype=dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("M,H", [(1, 8), (5, 24), (130, 4096), (64, 8192)])
+def test_norm_only(gnq, dtype, M, H):
+    x, r, w = _make(M, H, dtype, seed=5)
+    run_case(gnq, x, r, w, "none", 0.0, write_y=True, dtype=dtype)
+
+
+@pytest.mark.parametrize("k", [2, 3, 4, 5, 8])
+@pytest.mark.parametrize("mode,scale", [("nvfp4", 112.0), ("fp8", 0.05), ("none", 0.0)])
+def test_partials(gnq, k, mode, scale):
+    x, r, w = _make(150, 7168, "bf16", seed=k, k=k)
+    run_case(gnq, x, r, w, mode, scale, write_y=True, dtype="bf16")
+
+
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0)])
+def test_plain_rmsnorm_variant(gnq, mode, scale):
+    x, r, w = _make(100, 2048, "bf16", seed=3, w_std=1.0)
+    run_case(gnq, x, r, w, mode, scale, write_y=True, dtype="bf16", weight_bias=0.0)
+
+
+def test_odd_h_fp8(gnq):
+    # H a multiple of 8 but not of 16 or 64 (FP8 and the plain norm accept it)
+    x, r, w = _make(37, 8 * 129, "bf16", seed=1)
+    run_case(gnq, x, r, w, "fp8", 0.02, write_y=True, dtype="bf16")
+
+
+def test_max_h(gnq):
+    x, r, w = _make(3, 65536, "bf16", seed=2)
+    run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
+    run_case(gnq, x, r, w, "fp8", 0.05, write_y=False, dtype="bf16")
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("vpt", [1, 2, 4])
+def test_every_launch_shape(gnq, cluster, vpt):
+    """Forced cluster sizes and chunks per thread give the same contract."""
+    x, r, w = _make(133, 4096, "bf16", seed=cluster * 10 + vpt)
+    try:
+        gnq.set_launch_policy(cluster, vpt)
+        run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
+        run_case(gnq, x, r, w, "mxfp8", 0.0, write_y=False, dtype="bf16")
+        run_case(gnq, x, r, w, "fp8", 0.05, write_y=False, dtype="bf16")
+    finally:
+        gnq.set_launch_policy(0, 0)
+
+
+def test_special_rows(gnq):
+    """Zero rows, a weight of -1 (y is a signed zero), and tiny values."""
+    M, H = 8, 256
+    x = torch.randn(M, H).to(torch.bfloat16)
+    x[0] = 0.0
+    x[1] = 2.0 ** -120
+    x[2, ::2] = -x[2, ::2].abs()
+    r = torch.zeros(M, H, dtype=torch.bfloat16)
+    w = torch.randn(H).to(torch.bfloat16)
+    w[:32] = -1.0
+    for mode, s in (("fp8", 0.02), ("nvfp4", 168.0), ("mxfp8", 0.0)):
+        run_case(gnq, x, r, w, mode, s, write_y=True, dtype="bf16")
+
+
+def test_empty_batch(gnq):
+    dev = torch.device("cuda")
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device=dev)
+    w = torch.zeros(128, dtype=torch.bfloat16, device=dev)
+    s = torch.ones(1, dtype=torch.float32, device=dev)
+    q, bs, y = gnq.gemma_add_rms_norm_quant(x, None, w, 1e-6, s, "nvfp4", write_y=True)
+    assert q.shape == (0, 64) and bs.shape == (0, 8) and y.shape == (0, 128)
+
+
+def test_stream_and_graph_capture(gnq):
+    """A side stream and a captured CUDA graph give the eager results."""
+    dev = torch.device("cuda")
+    x, r, w = _make(256, 4096, "bf16", seed=9)
+    xd, wd = x.to(dev), w.to(dev)
+    sd = torch.tensor([0.05], device=dev)
+    r1 = r.to(dev)
+    q1, _, y1 = gnq.gemma_add_rms_norm_quant(xd, r1, wd, 1e-6, sd, "fp8", write_y=True)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    r2 = r.to(dev)
+    with torch.cuda.stream(side):
+        q2, _, y2 = gnq.gemma_add_rms_norm_quant(xd, r2, wd, 1e-6, sd, "fp8", write_y=True)
+    side.synchronize()
+    r3 = r.to(dev)
+    out = gnq.alloc_outputs(256, 4096, "fp8", True, xd)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        gnq.gemma_add_rms_norm_quant(xd, r3, wd, 1e-6, sd, "fp8", write_y=True, out=out)
+    r3.copy_(r.to(dev))
+    g.replay()
+    torch.cuda.synchronize()
+    for qq, yy, rr in ((q2, y2, r2), (out[0], out[2], r3)):
+        assert torch.equal(qq.view(torch.uint8), q1.view(torch.uint8))
+        assert torch.equal(yy, y1) and torch.equal(rr, r1)
+
+
+def test_status_codes_with_device_buffers(gnq):
+    lib = gnq.load()
+    import ctypes
+    dev = torch.device("cuda")
+    x = torch.zeros(4, 128, dtype=torch.bfloat16, device=dev)
+    r = torch.zeros(4, 128, dtype=torch.bfloat16, device=dev)
+    w = torch.zeros(128, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros(4, 128, dtype=torch.uint8, device=dev)
+    s = torch.ones(1, dtype=torch.float32, device=dev)
+    P = lambda t, off=0: ctypes.c_void_p(t.data_ptr() + off)
+    call = lib.gemma_add_rms_norm_quant
+    # x aliased with residual
+    assert call(P(x), P(x), P(w), 1e-6, P(s), 0, 0, P(q), None, None, 4, 128, 0, None) == 5
+    # misaligned x
+    assert call(P(x, 2), P(r), P(w), 1e-6, P(s), 0, 0, P(q), None, None, 3, 64, 0, None) == 6
+    # NVFP4 needs H % 64 == 0
+    assert call(P(x), P(r), P(w), 1e-6, P(s), 1, 0, P(q), P(q), None, 4, 96, 0, None) == 2
+    # missing scale / block scale
+    assert call(P(x), P(r), P(w), 1e-6, None, 0, 0, P(q), None, None, 4, 128, 0, None) == 1
+    assert call(P(x), P(r), P(w), 1e-6, P(s), 1, 0, P(q), None, None, 4, 128, 0, None) == 1
+    # bad dtype / mode
+    assert call(P(x), P(r), P(w), 1e-6, P(s), 0, 0, P(q), None, None, 4, 128, 7, None) == 3
+    assert call(P(x), P(r), P(w), 1e-6, P(s), 9, 0, P(q), None, None, 4, 128, 0, None) == 4
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(r) == 0  # rejected calls had no effect
