@@ -136,7 +136,7 @@ uint8_t or_e4m3_encode(double v) {
     uint8_t sign = signbit(v) ? 0x80 : 0x00;
     if (isnan(v)) return 0x7F | sign;
     double a = fabs(v);
-    if (isinf(a)) return sign | 0x7E;
+    if (a >= 448.0) return sign | 0x7E; /* saturate (infinity included) */
     int best = 0;
     double best_d = INFINITY;
     for (int c = 0; c <= 0x7E; ++c) { /* all finite non-negative codes */
@@ -163,11 +163,13 @@ double or_e2m1_value(uint8_t code) {
     return sign ? -v : v;
 }
 
-/* Nearest E2M1 value, ties to the even code, saturating at +-6; sign kept. */
+/* Nearest E2M1 value, ties to the even code, saturating at +-6; sign kept.
+ * Saturation is taken before the search: for huge |v| every distance rounds
+ * to the same double and the search alone would not find the largest code. */
 uint8_t or_e2m1_encode(double v) {
     uint8_t sign = signbit(v) ? 0x8 : 0x0;
     double a = fabs(v);
-    if (isinf(a)) return sign | 0x7;
+    if (a >= 6.0) return sign | 0x7; /* saturate (infinity included) */
     int best = 0;
     double best_d = INFINITY;
     for (int c = 0; c <= 0x7; ++c) {

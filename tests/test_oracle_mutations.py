@@ -31,6 +31,7 @@ MUTATIONS = [
     ("e4m3_ties_odd", "if (d < best_d || (d == best_d && (c & 1) == 0)) {\n            best = c;\n            best_d = d;\n        }\n    }\n    return (uint8_t)(sign | best);\n}\n\n/* ---",
      "if (d < best_d || (d == best_d && (c & 1) == 1)) {\n            best = c;\n            best_d = d;\n        }\n    }\n    return (uint8_t)(sign | best);\n}\n\n/* ---"),
     ("e2m1_no_saturation_sign", "uint8_t sign = signbit(v) ? 0x8 : 0x0;", "uint8_t sign = v < 0 ? 0x8 : 0x0;"),
+    ("e2m1_no_explicit_saturation", "if (a >= 6.0) return sign | 0x7;", "if (isinf(a)) return sign | 0x7;"),
     ("bf16_truncates", "double n = rint(a / ulp);", "double n = floor(a / ulp);"),
     ("mx_scale_off_by_one", "code = (e2 - 1) - 8 + 127;", "code = e2 - 8 + 127;"),
 ]
