@@ -155,16 +155,37 @@ int add_rms_norm_quant(const void *x_parts, int k, int64_t part_stride,
 const char *gnq_status_string(int status);
 
 /*
- * Tuning hook: force the launch shape of later calls in this process --
- * `cluster` CTAs per row (0 = automatic, else 1, 2, 4 or 8) and `vpt`
- * 16-byte chunks per thread (0 = automatic, else 1, 2 or 4).  A forced shape
- * that does not fit a call's H and mode is ignored for that call.  The shape
- * only changes the order in which a row's squares are summed (so y may move
- * by one rounding step); the residual, and the codes of a given y, do not
- * depend on it.  Not synchronised with calls in flight on other host
- * threads.  Returns GNQ_ERR_SHAPE for values outside those sets.
+ * Tuning hook: force the launch shape of later calls in this process.
+ *   kernel   0 = automatic; 1 = one CTA (or cluster) per row; 2 = persistent
+ *            streaming kernel (rows staged through shared memory).
+ *   cluster  row kernel only: 0 = automatic, else 1, 2, 4 or 8 CTAs per row.
+ *   vpt      0 = automatic, else 1, 2 or 4 16-byte chunks per thread.
+ * A forced shape that does not fit a call (H, mode, shared memory) falls back
+ * to the automatic one for that call.  The shape only changes the order in
+ * which a row's squares are summed (so y may move by one rounding step); the
+ * residual, and the codes of a given y, never depend on it.  Not
+ * synchronised with calls in flight on other host threads.  Returns
+ * GNQ_ERR_SHAPE for values outside those sets.
  */
-int gnq_set_launch_policy(int cluster, int vpt);
+int gnq_set_launch_policy(int kernel, int cluster, int vpt);
+
+/*
+ * Device error word of the current device.  Every wait inside a kernel is
+ * bounded; a kernel whose wait gives up (about a second without progress)
+ * skips the rest of its work, sets bit 1 here and returns, leaving its
+ * outputs incomplete.  Copies the word into *flags (synchronising the device)
+ * and clears it when `clear` is nonzero.
+ */
+int gnq_read_device_error(unsigned int *flags, int clear);
+
+/*
+ * Diagnostic: the static-FP8 quantizer the kernels use, applied to n fp32
+ * values y (device pointer): q[i] = e4m3_satfinite(y[i] / *scale), with
+ * `scale` a device pointer to one fp32.  Lets a test sweep every 16-bit y
+ * value against an independent encoder.
+ */
+int gnq_quantize_fp8_values(const float *y, int64_t n, const float *scale, uint8_t *q,
+                            void *stream);
 
 /*
  * Diagnostic: the element encoders the kernels use, applied to n fp32 values

@@ -12,6 +12,8 @@ from ._binding import (  # noqa: F401
     gemma_add_rms_norm_quant,
     gemma_add_rms_norm_quant_parts,
     library_path,
+    quantize_fp8_values,
+    read_device_error,
     load,
     set_launch_policy,
     status_string,

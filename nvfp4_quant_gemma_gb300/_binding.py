@@ -47,7 +47,9 @@ def load() -> ctypes.CDLL:
             "gemma_add_rms_norm_quant": [P, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "gemma_add_rms_norm_quant_parts": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "add_rms_norm_quant": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
-            "gnq_set_launch_policy": [I, I],
+            "gnq_set_launch_policy": [I, I, I],
+            "gnq_read_device_error": [P, I],
+            "gnq_quantize_fp8_values": [P, i64, P, P, P],
             "gnq_encode_e4m3_e2m1": [P, i64, P, P, P],
         }
         for name, argt in sigs.items():
@@ -63,7 +65,7 @@ def load() -> ctypes.CDLL:
 # Names the C ABI exports (checked by the test suite against include/gemma_nq.h).
 EXPORTS = ("gemma_add_rms_norm", "gemma_add_rms_norm_quant", "gemma_add_rms_norm_quant_parts",
            "add_rms_norm_quant", "gnq_status_string", "gnq_set_launch_policy",
-           "gnq_encode_e4m3_e2m1")
+           "gnq_read_device_error", "gnq_encode_e4m3_e2m1", "gnq_quantize_fp8_values")
 
 
 def status_string(status: int) -> str:
@@ -193,8 +195,29 @@ def add_rms_norm_quant(x_parts, residual, weight, eps, scale, mode, write_y=Fals
                        write_y, out, stream)
 
 
-def set_launch_policy(cluster: int = 0, vpt: int = 0) -> None:
-    _check(load().gnq_set_launch_policy(int(cluster), int(vpt)), "gnq_set_launch_policy")
+def set_launch_policy(kernel: int = 0, cluster: int = 0, vpt: int = 0) -> None:
+    """Force the launch shape (0 = automatic): kernel 1 = row kernel, 2 =
+    streaming kernel; cluster = CTAs per row; vpt = chunks per thread."""
+    _check(load().gnq_set_launch_policy(int(kernel), int(cluster), int(vpt)),
+           "gnq_set_launch_policy")
+
+
+def read_device_error(clear: bool = True) -> int:
+    """The device error word (bit 1: a bounded wait in a kernel gave up)."""
+    flags = ctypes.c_uint(0)
+    _check(load().gnq_read_device_error(ctypes.byref(flags), 1 if clear else 0),
+           "gnq_read_device_error")
+    return int(flags.value)
+
+
+def quantize_fp8_values(y: torch.Tensor, scale: torch.Tensor, stream=None) -> torch.Tensor:
+    """The kernels' static-FP8 quantizer on raw fp32 values (diagnostic)."""
+    if not (y.is_cuda and y.dtype == torch.float32 and y.is_contiguous()):
+        raise ValueError("y must be a contiguous fp32 CUDA tensor")
+    q = torch.empty(y.shape, dtype=torch.uint8, device=y.device)
+    _check(load().gnq_quantize_fp8_values(_ptr(y), y.numel(), _scale_ptr(scale), _ptr(q),
+                                          _stream(stream)), "gnq_quantize_fp8_values")
+    return q
 
 
 def encode_e4m3_e2m1(v: torch.Tensor, stream=None):

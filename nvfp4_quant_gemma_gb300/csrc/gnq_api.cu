@@ -22,20 +22,43 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kMaxH = 65536;
 constexpr int kMaxParts = 8;
 
-std::atomic<int> g_sm_count[kMaxDevices];  // 0 = not yet queried
+struct DevInfo {
+    int sms;
+    int smem_per_sm;    // bytes of shared memory per SM
+    int smem_optin;     // largest dynamic shared memory a CTA may opt in to
+    unsigned int *err;  // device address of the error word
+};
+
+// Error word written by kernels whose bounded waits gave up (bit
+// DEVERR_WAIT_TIMEOUT); one per device, read and cleared by
+// gnq_read_device_error.
+__device__ unsigned int g_device_error;
+
+std::atomic<int> g_ready[kMaxDevices];
+DevInfo g_info[kMaxDevices];
+std::atomic<int> g_force_kernel{0};  // 0 auto, 1 row kernel, 2 streaming kernel
 std::atomic<int> g_force_cluster{0};
 std::atomic<int> g_force_vpt{0};
 
-int sm_count() {
+// Device properties and the error word's address, queried once per device
+// with that device current.
+const DevInfo *dev_info() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
-    int n = g_sm_count[dev].load(std::memory_order_relaxed);
-    if (n == 0) {
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-        g_sm_count[dev].store(n, std::memory_order_relaxed);
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (g_ready[dev].load(std::memory_order_acquire) == 0) {
+        DevInfo d{};
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                   dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                   dev) != cudaSuccess ||
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_device_error) !=
+                cudaSuccess)
+            return nullptr;
+        g_info[dev] = d;  // identical values if two threads race here
+        g_ready[dev].store(1, std::memory_order_release);
     }
-    return n;
+    return &g_info[dev];
 }
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -44,37 +67,71 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // cluster may only split a row at multiples of this.
 int granule(int mode) { return mode == MODE_NVFP4 ? 64 : mode == MODE_MXFP8 ? 32 : 8; }
 
-bool shape_fits(int64_t H, int mode, int cluster, int vpt) {
+int max_threads(bool stream, int vpt) { return stream ? (vpt == 1 ? 1024 : 512) : 1024 / vpt; }
+
+bool row_shape_fits(int64_t H, int mode, int cluster, int vpt) {
     if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return false;
     if (vpt != 1 && vpt != 2 && vpt != 4) return false;
     if (H % ((int64_t)cluster * granule(mode)) != 0) return false;
-    const int64_t nch = H / cluster / 8;
-    const int64_t threads = (nch + vpt - 1) / vpt;
-    return threads <= 1024 / vpt;
+    const int64_t threads = (H / cluster / 8 + vpt - 1) / vpt;
+    return threads <= max_threads(false, vpt);
 }
 
-// Launch shape: rows are split over a cluster while the grid would otherwise
-// give fewer than ~4 CTAs per SM (small decode batches), then each CTA gets
-// enough chunks per thread to stay within 512 threads.
-LaunchShape choose_shape(int64_t M, int64_t H, int mode) {
-    const int sms = sm_count();
-    LaunchShape ls{1, 1, 32};
-    while (ls.cluster < 8 && M * ls.cluster < 4LL * sms &&
+// Streaming kernel shape: CTAs per SM and ring depth from the shared memory
+// a row needs (operands x 2H bytes per stage); false if it does not fit.
+bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int nops, int vpt, LaunchShape &ls) {
+    if (vpt != 1 && vpt != 2 && vpt != 4) return false;
+    const int64_t threads = (H / 8 + vpt - 1) / vpt;
+    if (threads > max_threads(true, vpt)) return false;
+    const int64_t stage = (int64_t)nops * 2 * H;
+    if (stage >= (1 << 20)) return false;  // mbarrier transaction count limit
+    const int64_t reserve = 1024 + 2048;   // per-CTA system reserve + static shared memory
+    for (int ctas = 2; ctas >= 1; --ctas) {
+        int64_t budget = d.smem_per_sm / ctas - reserve;
+        if (budget > d.smem_optin) budget = d.smem_optin;
+        int64_t S = budget / stage;
+        if (S > 4) S = 4;
+        if (S >= 2) {
+            ls.stream = true;
+            ls.cluster = 1;
+            ls.vpt = vpt;
+            ls.threads = (int)((threads + 31) / 32 * 32);
+            ls.stages = (int)S;
+            ls.smem = (size_t)(stage * S + 8 * S);
+            ls.grid = M < (int64_t)d.sms * ctas ? M : (int64_t)d.sms * ctas;
+            return true;
+        }
+    }
+    return false;
+}
+
+// Launch shape.  Large batches (M >= 2 x SMs) stream rows through persistent
+// CTAs; smaller ones give each row a CTA, split over a cluster while the grid
+// would otherwise have fewer than ~4 CTAs per SM.  Chunks per thread keep a
+// CTA within 512 threads.
+LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops) {
+    const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
+    LaunchShape ls{false, 1, 1, 32, M, 0, 0};
+    const int vpt_stream = H <= 4096 ? 1 : H <= 8192 ? 2 : 4;
+    const bool want_stream = fk == 2 || (fk == 0 && M >= 2LL * d.sms);
+    if (want_stream && stream_shape(d, M, H, nops, fv ? fv : vpt_stream, ls)) return ls;
+    if (want_stream && fv && stream_shape(d, M, H, nops, vpt_stream, ls)) return ls;
+
+    while (ls.cluster < 8 && M * ls.cluster < 4LL * d.sms &&
            H % (2LL * ls.cluster * granule(mode)) == 0 && H / (2 * ls.cluster) >= 256)
         ls.cluster *= 2;
     const int64_t nch = H / ls.cluster / 8;
     while (ls.vpt < 4 && (nch + ls.vpt - 1) / ls.vpt > 512) ls.vpt *= 2;
-    const int fc = g_force_cluster.load(), fv = g_force_vpt.load();
     if (fc || fv) {
         const int c = fc ? fc : ls.cluster, v = fv ? fv : ls.vpt;
-        if (shape_fits(H, mode, c, v)) {
+        if (row_shape_fits(H, mode, c, v)) {
             ls.cluster = c;
             ls.vpt = v;
         }
     }
-    const int64_t n = H / ls.cluster / 8;
-    const int64_t threads = (n + ls.vpt - 1) / ls.vpt;
+    const int64_t threads = (H / ls.cluster / 8 + ls.vpt - 1) / ls.vpt;
     ls.threads = (int)((threads + 31) / 32 * 32);
+    ls.grid = M * ls.cluster;
     return ls;
 }
 
@@ -123,8 +180,12 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     p.Kp4 = (int)(((H / 16) + 3) / 4);
     p.write_y = write_y ? 1 : 0;
 
-    const LaunchShape ls = choose_shape(M, H, mode);
+    const DevInfo *d = dev_info();
+    if (!d) return GNQ_ERR_CUDA;
+    const LaunchShape ls = choose_shape(*d, M, H, mode, k + (residual ? 1 : 0));
     p.seg = (int)(H / ls.cluster);
+    p.stages = ls.stages;
+    p.err = d->err;
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool parts = k > 1;
@@ -136,6 +197,13 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
         default: e = launch_mode<MODE_MXFP8>(p, dtype, parts, ls, s); break;
     }
     return e == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
+}
+
+__global__ void fp8_values_kernel(const float *y, int64_t n, const float *scale, uint8_t *q) {
+    const Fp8Div fd = make_fp8_div(*scale);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        q[i] = (uint8_t)(e4m3x2(fp8_quotient(y[i], fd), 0.f) & 0xFF);
 }
 
 __global__ void encode_kernel(const float *v, int64_t n, uint8_t *e4m3, uint8_t *e2m1) {
@@ -198,11 +266,23 @@ const char *gnq_status_string(int status) {
     }
 }
 
-int gnq_set_launch_policy(int cluster, int vpt) {
+int gnq_set_launch_policy(int kernel, int cluster, int vpt) {
+    if (kernel < 0 || kernel > 2) return GNQ_ERR_SHAPE;
     if (cluster < 0 || cluster > 8 || (cluster & (cluster - 1))) return GNQ_ERR_SHAPE;
     if (vpt != 0 && vpt != 1 && vpt != 2 && vpt != 4) return GNQ_ERR_SHAPE;
+    gnq::g_force_kernel.store(kernel);
     gnq::g_force_cluster.store(cluster);
     gnq::g_force_vpt.store(vpt);
+    return GNQ_OK;
+}
+
+int gnq_read_device_error(unsigned int *flags, int clear) {
+    if (!flags) return GNQ_ERR_NULL;
+    const gnq::DevInfo *d = gnq::dev_info();
+    if (!d) return GNQ_ERR_CUDA;
+    if (cudaMemcpy(flags, d->err, sizeof(unsigned int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GNQ_ERR_CUDA;
+    if (clear && cudaMemset(d->err, 0, sizeof(unsigned int)) != cudaSuccess) return GNQ_ERR_CUDA;
     return GNQ_OK;
 }
 
@@ -214,6 +294,17 @@ int gnq_encode_e4m3_e2m1(const float *v, int64_t n, uint8_t *e4m3, uint8_t *e2m1
     const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
     gnq::encode_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         v, n, e4m3, e2m1);
+    return cudaGetLastError() == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
+}
+
+int gnq_quantize_fp8_values(const float *y, int64_t n, const float *scale, uint8_t *q,
+                            void *stream) {
+    if (n < 0) return GNQ_ERR_SHAPE;
+    if (n == 0) return GNQ_OK;
+    if (!y || !scale || !q) return GNQ_ERR_NULL;
+    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    gnq::fp8_values_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        y, n, scale, q);
     return cudaGetLastError() == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
 }
 

@@ -1,0 +1,300 @@
+// Device building blocks of the fused add + Gemma RMSNorm + quant kernels
+// (sm_103a): vector memory access, 16-bit activation packing, the hardware
+// FP8/FP4 encoders, exact quotients, cluster and bulk-copy/mbarrier helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gnq {
+
+enum { MODE_NONE = -1, MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_MXFP8 = 2 };
+
+// Bits of the device error word (set by a kernel, read by gnq_device_error).
+enum { DEVERR_WAIT_TIMEOUT = 1 };
+
+struct Params {
+    const uint16_t *x;    // the activation, or partial 0 of k
+    int64_t part_stride;  // elements from one partial to the next
+    int k;                // number of partials (1 = plain activation)
+    uint16_t *residual;   // (M, H) or nullptr; updated in place
+    const uint16_t *w;    // (H,)
+    float eps;
+    float weight_bias;    // 1 for the Gemma norm, 0 for a plain RMSNorm
+    const float *scale;   // device fp32: FP8 scale or NVFP4 global scale
+    uint8_t *q;
+    uint8_t *block_scale;
+    uint16_t *y;          // (M, H) or nullptr
+    int64_t M;
+    int H;
+    int Kp4;              // NVFP4: round_up(H/16, 4) / 4 scale tiles per 128 rows
+    int seg;              // elements owned by one CTA (H / cluster size)
+    int write_y;
+    int stages;           // streaming kernel: rows in flight per CTA
+    unsigned int *err;    // device error word
+};
+
+// ---------------------------------------------------------------------------
+// global memory (16-byte vectors; cache hints for a one-pass stream)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 r;  // read-only input touched once: no L1 allocation
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_inout(const void *p) {
+    uint4 r;  // the residual: read, then overwritten by the same thread
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_weight(const void *p) {
+    uint4 r;  // the norm weight is re-read by every row: keep it in L1
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ void st_v4(void *p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_v2(void *p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void st_u32(void *p, uint32_t a) {
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+__device__ __forceinline__ void st_u8(void *p, uint32_t a) {
+    asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(a) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+    uint4 r;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "r"(addr));
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// 16-bit activation types: 8 values <-> one uint4
+// ---------------------------------------------------------------------------
+template <typename T> struct Act;
+
+template <> struct Act<__nv_bfloat16> {
+    static __device__ __forceinline__ void unpack(uint4 v, float f[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
+    }
+    static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<uint32_t *>(&b);
+    }
+};
+
+template <> struct Act<__half> {
+    static __device__ __forceinline__ void unpack(uint4 v, float f[8]) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+            float2 p = __half22float2(h);
+            f[2 * i] = p.x;
+            f[2 * i + 1] = p.y;
+        }
+    }
+    static __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);  // round to nearest even
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+};
+
+template <typename T> __device__ __forceinline__ uint4 pack8(const float f[8]) {
+    uint4 r;
+    r.x = Act<T>::pack2(f[0], f[1]);
+    r.y = Act<T>::pack2(f[2], f[3]);
+    r.z = Act<T>::pack2(f[4], f[5]);
+    r.w = Act<T>::pack2(f[6], f[7]);
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// element encoders (hardware conversions, round to nearest even, saturating)
+// ---------------------------------------------------------------------------
+// Two E4M3 codes in 16 bits, `lo` in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+
+// Four E2M1 codes in 16 bits: element 0 in bits 0-3, element 1 in 4-7, ...
+__device__ __forceinline__ uint32_t e2m1x4(float v0, float v1, float v2, float v3) {
+    uint16_t d;
+    asm("{\n\t.reg .b8 lo8, hi8;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 lo8, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 hi8, %4, %3;\n\t"
+        "mov.b16 %0, {lo8, hi8};\n\t}"
+        : "=h"(d)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return d;
+}
+
+// Value of an E4M3 code (bias 7, 3 fraction bits; S.1111.111 is NaN), exact in fp32.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    const uint32_t e = (code >> 3) & 0xF, f = code & 0x7;
+    float mag = e ? __uint_as_float(((e + 120u) << 23) | (f << 20))  // (1+f/8)*2^(e-7)
+                  : (float)f * 0.001953125f;                          // f/8 * 2^-6
+    if (e == 0xF && f == 0x7) mag = __uint_as_float(0x7FC00000u);
+    return (code & 0x80) ? -mag : mag;
+}
+
+// ---------------------------------------------------------------------------
+// exact quotients
+// ---------------------------------------------------------------------------
+// Correctly rounded a / b from r = RN(1/b) with the FMA correction step of
+// P. W. Markstein ("Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(a*r) is
+// within one ulp of a/b, the remainder a - q0*b is then exact in one fused
+// multiply-add, and RN(q0 + rem*r) is the correctly rounded quotient.
+// Requires b and r normal and |a| >= 2^-103 (so the remainder cannot
+// underflow); a zero or non-finite q0 is returned as is.
+__device__ __forceinline__ float div_fma(float a, float b, float r, float &q0) {
+    q0 = __fmul_rn(a, r);
+    const float rem = __fmaf_rn(-q0, b, a);
+    return __fmaf_rn(rem, r, q0);
+}
+
+// The static FP8 quotient y / s as the E4M3 encoder needs it.  With
+// 2^-80 <= |s| <= 2^80 (`fast`): quotients of magnitude 512 or more
+// saturate to 448 whatever their last bits (q0 is kept, which also covers
+// infinities); |y| < 2^-103 gives |y/s| < 2^-23, a signed zero code either
+// way; zero q0 carries the sign of y/s.  Other scales take the IEEE division.
+struct Fp8Div {
+    float s, r;
+    bool fast;
+};
+
+__device__ __forceinline__ Fp8Div make_fp8_div(float s) {
+    Fp8Div d;
+    d.s = s;
+    d.r = __frcp_rn(s);
+    const float a = fabsf(s);
+    d.fast = a >= 0x1p-80f && a <= 0x1p80f;
+    return d;
+}
+
+__device__ __forceinline__ float fp8_quotient(float y, const Fp8Div &d) {
+    if (!d.fast) return __fdiv_rn(y, d.s);
+    float q0;
+    const float q1 = div_fma(y, d.s, d.r, q0);
+    return (fabsf(q0) >= 512.f || q0 == 0.f) ? q0 : q1;
+}
+
+// amax / 6 correctly rounded (amax >= 0).
+__device__ __forceinline__ float div6(float amax) {
+    if (!(amax >= 0x1p-100f) || amax > 0x1p120f) return __fdiv_rn(amax, 6.0f);
+    float q0;
+    const float q1 = div_fma(amax, 6.0f, 0.16666667163372039794921875f /* RN(1/6) */, q0);
+    return q1;
+}
+
+// ---------------------------------------------------------------------------
+// cluster helpers (distributed shared memory)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_size() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_peer_f32(const float *local, uint32_t rank) {
+    uint32_t a = (uint32_t)__cvta_generic_to_shared(local), ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// bulk copies into shared memory, completed on an mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait: gives up after ~2^31 cycles (about a second) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (1LL << 31)) return false;
+    }
+    return true;
+}
+// 1-D bulk copy global -> this CTA's shared memory; bytes and both
+// addresses are multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Byte offset of block scale (m, b) in the 128x4 swizzled layout, for b % 4 == 0.
+__device__ __forceinline__ int64_t swizzled_group(int64_t m, int b, int Kp4) {
+    return ((m >> 7) * Kp4 + (b >> 2)) * 512 + (m & 31) * 16 + ((m >> 5) & 3) * 4;
+}
+
+}  // namespace gnq

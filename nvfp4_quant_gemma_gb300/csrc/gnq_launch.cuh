@@ -1,7 +1,8 @@
-// Launch of the row kernel for one quantization mode: picks the template
-// instance (activation type, partials or not, chunks per thread) and applies
-// the cluster size as a launch attribute.  One translation unit per mode
-// instantiates it, so the library builds in parallel.
+// Launch of the kernels for one quantization mode: picks the template
+// instance (kernel kind, activation type, partials or not, chunks per thread)
+// and applies the cluster size or the dynamic shared memory size.  One
+// translation unit per mode instantiates it, so the library builds in
+// parallel.
 #pragma once
 
 #include "gnq_kernels.cuh"
@@ -9,40 +10,49 @@
 namespace gnq {
 
 struct LaunchShape {
-    int cluster;  // CTAs per row (1, 2, 4, 8)
-    int vpt;      // 16-byte chunks per thread (1, 2, 4)
-    int threads;  // threads per CTA, a multiple of 32
+    bool stream;     // persistent streaming kernel (else one CTA/cluster per row)
+    int cluster;     // row kernel: CTAs per row (1, 2, 4, 8)
+    int vpt;         // 16-byte chunks per thread (1, 2, 4)
+    int threads;     // threads per CTA, a multiple of 32
+    int64_t grid;    // CTAs
+    int stages;      // streaming kernel: rows in flight per CTA
+    size_t smem;     // streaming kernel: dynamic shared memory bytes
 };
 
 template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream);
 
-#define GNQ_PICK(T, VPT)                                                          \
-    (parts ? (void (*)(const Params))row_kernel<T, MODE, true, VPT>               \
-           : (void (*)(const Params))row_kernel<T, MODE, false, VPT>)
+#define GNQ_PICK(K, T, VPT)                                                   \
+    (parts ? (void (*)(const Params))K<T, MODE, true, VPT>                     \
+           : (void (*)(const Params))K<T, MODE, false, VPT>)
+
+#define GNQ_PICK_VPT(K, T)                                                    \
+    (ls.vpt == 1 ? GNQ_PICK(K, T, 1) : ls.vpt == 2 ? GNQ_PICK(K, T, 2) : GNQ_PICK(K, T, 4))
 
 template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream) {
     void (*fn)(const Params) = nullptr;
-    if (dtype == 0) {
-        fn = ls.vpt == 1 ? GNQ_PICK(__nv_bfloat16, 1)
-           : ls.vpt == 2 ? GNQ_PICK(__nv_bfloat16, 2)
-                         : GNQ_PICK(__nv_bfloat16, 4);
+    if (ls.stream) {
+        fn = dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
+                        : GNQ_PICK_VPT(stream_kernel, __half);
+        // opt in to the dynamic shared memory this launch needs (idempotent)
+        const cudaError_t e = cudaFuncSetAttribute(
+            fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem);
+        if (e != cudaSuccess) return e;
     } else {
-        fn = ls.vpt == 1 ? GNQ_PICK(__half, 1)
-           : ls.vpt == 2 ? GNQ_PICK(__half, 2)
-                         : GNQ_PICK(__half, 4);
+        fn = dtype == 0 ? GNQ_PICK_VPT(row_kernel, __nv_bfloat16)
+                        : GNQ_PICK_VPT(row_kernel, __half);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.M * ls.cluster), 1, 1);
+    cfg.gridDim = dim3((unsigned)ls.grid, 1, 1);
     cfg.blockDim = dim3((unsigned)ls.threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = ls.stream ? ls.smem : 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     cfg.numAttrs = 0;
-    if (ls.cluster > 1) {
+    if (!ls.stream && ls.cluster > 1) {
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = (unsigned)ls.cluster;
         attr[0].val.clusterDim.y = 1;
@@ -53,6 +63,7 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+#undef GNQ_PICK_VPT
 #undef GNQ_PICK
 
 }  // namespace gnq

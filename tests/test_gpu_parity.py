@@ -34,7 +34,7 @@ def gnq():
     build.build()
     import nvfp4_quant_gemma_gb300 as pkg
     pkg.load()
-    pkg.set_launch_policy(0, 0)
+    pkg.set_launch_policy(0, 0, 0)
     oracle.build()
     import os
     oracle.set_threads(os.cpu_count() or 1)
@@ -234,18 +234,73 @@ def test_max_h(gnq):
     run_case(gnq, x, r, w, "fp8", 0.05, write_y=False, dtype="bf16")
 
 
-@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
-@pytest.mark.parametrize("vpt", [1, 2, 4])
-def test_every_launch_shape(gnq, cluster, vpt):
-    """Forced cluster sizes and chunks per thread give the same contract."""
-    x, r, w = _make(133, 4096, "bf16", seed=cluster * 10 + vpt)
-    try:
-        gnq.set_launch_policy(cluster, vpt)
+class forced_policy:
+    def __init__(self, gnq, kernel, cluster=0, vpt=0):
+        self.gnq, self.args = gnq, (kernel, cluster, vpt)
+
+    def __enter__(self):
+        self.gnq.set_launch_policy(*self.args)
+
+    def __exit__(self, *exc):
+        self.gnq.set_launch_policy(0, 0, 0)
+
+
+@pytest.mark.parametrize("kernel,cluster,vpt", [(1, c, v) for c in (1, 2, 4, 8) for v in (1, 2, 4)]
+                         + [(2, 0, v) for v in (1, 2, 4)])
+def test_every_launch_shape(gnq, kernel, cluster, vpt):
+    """Forced kernels, cluster sizes and chunks per thread give the same contract."""
+    x, r, w = _make(133, 4096, "bf16", seed=cluster * 10 + vpt + kernel)
+    with forced_policy(gnq, kernel, cluster, vpt):
         run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
         run_case(gnq, x, r, w, "mxfp8", 0.0, write_y=False, dtype="bf16")
         run_case(gnq, x, r, w, "fp8", 0.05, write_y=False, dtype="bf16")
-    finally:
-        gnq.set_launch_policy(0, 0)
+    assert gnq.read_device_error() == 0
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.08), ("nvfp4", 84.0), ("mxfp8", 0.0), ("none", 0.0)])
+@pytest.mark.parametrize("M,H,k,res", [(1, 64, 1, True), (7, 2048, 1, False), (333, 5120, 1, True),
+                                       (1000, 8192, 1, True), (610, 7168, 4, True),
+                                       (300, 16384, 1, True), (160, 1024, 3, False)])
+def test_streaming_kernel(gnq, dtype, mode, scale, M, H, k, res):
+    """The persistent shared-memory-ring kernel on ragged row counts (rows per
+    CTA differ), every mode, with and without residual and partials."""
+    x, r, w = _make(M, H, dtype, seed=M + H + k, k=k, residual=res)
+    with forced_policy(gnq, 2):
+        run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 0), dtype=dtype,
+                 check_e2e=(M * H >= 1e5))
+    assert gnq.read_device_error() == 0
+
+
+def test_automatic_policy_large_batch(gnq):
+    """The automatic choice for a prefill-sized batch (streaming kernel)."""
+    x, r, w = _make(2048, 5120, "bf16", seed=77)
+    run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
+    assert gnq.read_device_error() == 0
+
+
+def _all_finite_16bit(dtype):
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = torch.from_numpy(pats.view(np.int16)).view(DTYPES[dtype]).float()
+    return v[torch.isfinite(v)].contiguous()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fp8_quotient_every_16bit_value(gnq, dtype):
+    """The kernels' y / s (FMA-corrected reciprocal path, IEEE division for
+    extreme scales) against the oracle on every finite 16-bit y."""
+    y = _all_finite_16bit(dtype)
+    yd = y.cuda()
+    rng = np.random.default_rng(5)
+    scales = [0.02, 0.05, 0.08, 1.0, 0.03, 3.0, 448.0, 2.0 ** -80, 2.0 ** 80, 2.0 ** -81,
+              1e-30, 1e30, -0.05, 7e-5]
+    scales += list(np.exp(rng.uniform(np.log(1e-4), np.log(1e4), 40)))
+    y64 = y.double().numpy()
+    for s in scales:
+        s32 = np.float32(s)
+        q = gnq.quantize_fp8_values(yd, torch.tensor([s32], device="cuda")).cpu().numpy()
+        ref = oracle.e4m3_encode((y.numpy() / s32).astype(np.float64))  # fp32 IEEE division
+        assert np.array_equal(q, ref), f"scale {s}"
 
 
 def test_special_rows(gnq):
