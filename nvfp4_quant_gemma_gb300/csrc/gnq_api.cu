@@ -170,6 +170,7 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     p.residual = static_cast<uint16_t *>(residual);
     p.w = static_cast<const uint16_t *>(w);
     p.eps = eps;
+    p.inv_h = 1.0f / (float)H;
     p.weight_bias = weight_bias;
     p.scale = scale;
     p.q = static_cast<uint8_t *>(q);
@@ -202,8 +203,10 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 __global__ void fp8_values_kernel(const float *y, int64_t n, const float *scale, uint8_t *q) {
     const Fp8Div fd = make_fp8_div(*scale);
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x)
-        q[i] = (uint8_t)(e4m3x2(fp8_quotient(y[i], fd), 0.f) & 0xFF);
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const float d = fd.fast ? fp8_quotient<true>(y[i], fd) : fp8_quotient<false>(y[i], fd);
+        q[i] = (uint8_t)(e4m3x2(d, 0.f) & 0xFF);
+    }
 }
 
 __global__ void encode_kernel(const float *v, int64_t n, uint8_t *e4m3, uint8_t *e2m1) {

@@ -22,6 +22,7 @@ struct Params {
     uint16_t *residual;   // (M, H) or nullptr; updated in place
     const uint16_t *w;    // (H,)
     float eps;
+    float inv_h;          // RN(1 / H)
     float weight_bias;    // 1 for the Gemma norm, 0 for a plain RMSNorm
     const float *scale;   // device fp32: FP8 scale or NVFP4 global scale
     uint8_t *q;
@@ -142,6 +143,18 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     return d;
 }
 
+// Four E4M3 codes in 32 bits, element 0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3x4(float v0, float v1, float v2, float v3) {
+    uint32_t d;
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 a, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 b, %4, %3;\n\t"
+        "mov.b32 %0, {a, b};\n\t}"
+        : "=r"(d)
+        : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return d;
+}
+
 // Four E2M1 codes in 16 bits: element 0 in bits 0-3, element 1 in 4-7, ...
 __device__ __forceinline__ uint32_t e2m1x4(float v0, float v1, float v2, float v3) {
     uint16_t d;
@@ -151,6 +164,22 @@ __device__ __forceinline__ uint32_t e2m1x4(float v0, float v1, float v2, float v
         "mov.b16 %0, {lo8, hi8};\n\t}"
         : "=h"(d)
         : "f"(v0), "f"(v1), "f"(v2), "f"(v3));
+    return d;
+}
+
+// Eight E2M1 codes in 32 bits, element i in bits 4i..4i+3.
+__device__ __forceinline__ uint32_t e2m1x8(const float v[8]) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 c3, %8, %7;\n\t"
+        "mov.b16 lo, {c0, c1};\n\t"
+        "mov.b16 hi, {c2, c3};\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(d)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
     return d;
 }
 
@@ -179,13 +208,15 @@ __device__ __forceinline__ float div_fma(float a, float b, float r, float &q0) {
     return __fmaf_rn(rem, r, q0);
 }
 
-// The static FP8 quotient y / s as the E4M3 encoder needs it.  With
-// 2^-80 <= |s| <= 2^80 (`fast`): quotients of magnitude 512 or more
-// saturate to 448 whatever their last bits (q0 is kept, which also covers
-// infinities); |y| < 2^-103 gives |y/s| < 2^-23, a signed zero code either
-// way; zero q0 carries the sign of y/s.  Other scales take the IEEE division.
+// The static FP8 quotient y / s as the E4M3 encoder needs it.  `fast` holds
+// for 2^-80 <= s <= 2^80 (s positive): then |y| is first clamped to
+// ylim = 1024 s (a clamped quotient is >= 1024 and saturates to 448, like
+// the true one; NaN passes through), the quotient of |y| is taken with the
+// FMA correction (exact for |y| >= 2^-103; below that |y/s| < 2^-23, a zero
+// code either way), and the sign of y is put back -- which also gives -0 for
+// y = -0.  Other scales take the IEEE division.
 struct Fp8Div {
-    float s, r;
+    float s, r, ylim;
     bool fast;
 };
 
@@ -193,16 +224,24 @@ __device__ __forceinline__ Fp8Div make_fp8_div(float s) {
     Fp8Div d;
     d.s = s;
     d.r = __frcp_rn(s);
-    const float a = fabsf(s);
-    d.fast = a >= 0x1p-80f && a <= 0x1p80f;
+    d.ylim = s * 1024.f;  // exact: power-of-two scaling in range
+    d.fast = s >= 0x1p-80f && s <= 0x1p80f;
     return d;
 }
 
+__device__ __forceinline__ float min_nan(float a, float b) {
+    float d;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+template <bool FAST>
 __device__ __forceinline__ float fp8_quotient(float y, const Fp8Div &d) {
-    if (!d.fast) return __fdiv_rn(y, d.s);
+    if (!FAST) return __fdiv_rn(y, d.s);
+    const float a = min_nan(fabsf(y), d.ylim);
     float q0;
-    const float q1 = div_fma(y, d.s, d.r, q0);
-    return (fabsf(q0) >= 512.f || q0 == 0.f) ? q0 : q1;
+    const float q = div_fma(a, d.s, d.r, q0);
+    return copysignf(q, y);
 }
 
 // amax / 6 correctly rounded (amax >= 0).

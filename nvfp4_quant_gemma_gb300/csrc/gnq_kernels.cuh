@@ -32,6 +32,8 @@
 // (see gnq_device.cuh), so codes are exactly those of the fp32 reading.
 #pragma once
 
+#include <type_traits>
+
 #include "gnq_device.cuh"
 
 namespace gnq {
@@ -53,7 +55,8 @@ __device__ __forceinline__ void fill_es_table(float *tab, float g, int t, int nt
 
 // y for one chunk (8 values of y before rounding), then the quantizer and the
 // stores.  `t` is the thread index (lane groups for the scale gathers).
-template <typename T, int MODE>
+// FAST selects the FP8 quotient path (uniform per CTA, see Fp8Div).
+template <typename T, int MODE, bool FAST>
 __device__ __forceinline__ void epilogue_chunk(const Params &p, const QuantCtx &qc, float yf[8],
                                                int64_t m, int64_t row, int col, bool ok, int t) {
     const uint4 yb = pack8<T>(yf);
@@ -63,9 +66,9 @@ __device__ __forceinline__ void epilogue_chunk(const Params &p, const QuantCtx &
     if (MODE == MODE_FP8) {
         float d[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) d[i] = fp8_quotient(yf[i], qc.fd);
-        const uint32_t lo = e4m3x2(d[0], d[1]) | (e4m3x2(d[2], d[3]) << 16);
-        const uint32_t hi = e4m3x2(d[4], d[5]) | (e4m3x2(d[6], d[7]) << 16);
+        for (int i = 0; i < 8; ++i) d[i] = fp8_quotient<FAST>(yf[i], qc.fd);
+        const uint32_t lo = e4m3x4(d[0], d[1], d[2], d[3]);
+        const uint32_t hi = e4m3x4(d[4], d[5], d[6], d[7]);
         if (ok) st_v2(p.q + row + col, lo, hi);
     } else if (MODE == MODE_NVFP4) {
         float amax = 0.f;
@@ -77,8 +80,7 @@ __device__ __forceinline__ void epilogue_chunk(const Params &p, const QuantCtx &
         const float es = qc.es_tab[sf];
 #pragma unroll
         for (int i = 0; i < 8; ++i) yf[i] = __fmul_rn(yf[i], es);
-        const uint32_t codes = e2m1x4(yf[0], yf[1], yf[2], yf[3]) |
-                               (e2m1x4(yf[4], yf[5], yf[6], yf[7]) << 16);
+        const uint32_t codes = e2m1x8(yf);
         if (ok) st_u32(p.q + ((row + col) >> 1), codes);
         // scale bytes of 4 consecutive blocks (lanes 8i, 8i+2, 8i+4, 8i+6)
         const uint32_t s1 = __shfl_down_sync(0xffffffffu, sf, 2);
@@ -100,12 +102,24 @@ __device__ __forceinline__ void epilogue_chunk(const Params &p, const QuantCtx &
         float d[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) d[i] = __fmul_rn(yf[i], inv_x);
-        const uint32_t lo = e4m3x2(d[0], d[1]) | (e4m3x2(d[2], d[3]) << 16);
-        const uint32_t hi = e4m3x2(d[4], d[5]) | (e4m3x2(d[6], d[7]) << 16);
+        const uint32_t lo = e4m3x4(d[0], d[1], d[2], d[3]);
+        const uint32_t hi = e4m3x4(d[4], d[5], d[6], d[7]);
         if (ok) st_v2(p.q + row + col, lo, hi);
         if (ok && (t & 3) == 0)
             st_u8(p.block_scale + m * (int64_t)(p.H >> 5) + (col >> 5), (uint32_t)code);
     }
+}
+
+// Sum of the per-warp partials in warp_ss[0..nw): each warp reduces them
+// with the same shuffle tree, so every thread gets the same value.
+__device__ __forceinline__ float block_total(const float *warp_ss, int nw, int lane) {
+    float v = lane < nw ? warp_ss[lane] : 0.f;
+    return warp_sum(v);
+}
+
+// inv = 1 / sqrt(mean(h^2) + eps); mean via the host-rounded 1/H.
+__device__ __forceinline__ float inv_rms(const Params &p, float tot) {
+    return rsqrtf(__fadd_rn(__fmul_rn(tot, p.inv_h), p.eps));
 }
 
 __device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, float *es_smem,
@@ -216,8 +230,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     ss = warp_sum(ss);
     if ((t & 31) == 0) warp_ss[t >> 5] = ss;
     __syncthreads();
-    float tot = 0.f;
-    for (int i = 0; i < (NT >> 5); ++i) tot += warp_ss[i];
+    float tot = block_total(warp_ss, NT >> 5, t & 31);
     if (C > 1) {
         if (t == 0) cta_ss = tot;
         cluster_arrive_release();
@@ -226,18 +239,22 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
         for (uint32_t r = 0; r < C; ++r) tot += ld_peer_f32(&cta_ss, r);
         cluster_arrive_relaxed();  // this CTA's reads of its peers are done
     }
-    const float inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)p.H), p.eps));
+    const float inv = inv_rms(p, tot);
 
     // ---- y = dtype(h * inv * (bias + w)), then quantize the rounded y ----
+    auto finish = [&](auto fast) {
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        float wf[8], yf[8];
-        Act<T>::unpack(wv[v], wf);
+        for (int v = 0; v < VPT; ++v) {
+            float wf[8], yf[8];
+            Act<T>::unpack(wv[v], wf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            yf[i] = __fmul_rn(__fmul_rn(h[v][i], inv), __fadd_rn(p.weight_bias, wf[i]));
-        epilogue_chunk<T, MODE>(p, qc, yf, m, row, col[v], ok[v], t);
-    }
+            for (int i = 0; i < 8; ++i)
+                yf[i] = __fmul_rn(__fmul_rn(h[v][i], inv), __fadd_rn(p.weight_bias, wf[i]));
+            epilogue_chunk<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+        }
+    };
+    if (MODE != MODE_FP8 || qc.fd.fast) finish(std::true_type{});
+    else finish(std::false_type{});
 
     if (C > 1) cluster_wait();  // peers may still be reading this CTA's partial
 }
@@ -361,17 +378,19 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
             fence_async_shared();
             issue(i + S);
         }
-        float tot = 0.f;
-        for (int w = 0; w < (NT >> 5); ++w) tot += warp_ss[i & 1][w];
-        const float inv = __frsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)p.H), p.eps));
+        const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
 
+        auto finish = [&](auto fast) {
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            float yf[8];
+            for (int v = 0; v < VPT; ++v) {
+                float yf[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) yf[e] = __fmul_rn(__fmul_rn(h[v][e], inv), bw[v][e]);
-            epilogue_chunk<T, MODE>(p, qc, yf, m, row, col[v], ok[v], t);
-        }
+                for (int e = 0; e < 8; ++e) yf[e] = __fmul_rn(__fmul_rn(h[v][e], inv), bw[v][e]);
+                epilogue_chunk<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+            }
+        };
+        if (MODE != MODE_FP8 || qc.fd.fast) finish(std::true_type{});
+        else finish(std::false_type{});
     }
 }
 
