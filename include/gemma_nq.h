@@ -170,6 +170,16 @@ const char *gnq_status_string(int status);
 int gnq_set_launch_policy(int kernel, int cluster, int vpt);
 
 /*
+ * Programmatic dependent launch (on by default): each launch may start while
+ * the preceding kernel on the stream drains, and waits inside the kernel
+ * (griddepcontrol.wait) until that kernel's results are visible before its
+ * first global read; a launch that fits the GPU in one wave also lets the
+ * kernel that follows it start early.  Results are identical either way.
+ * enable = 0 turns it off for later calls in this process, 1 turns it on.
+ */
+int gnq_set_pdl(int enable);
+
+/*
  * Device error word of the current device.  Every wait inside a kernel is
  * bounded; a kernel whose wait gives up (about a second without progress)
  * skips the rest of its work, sets bit 1 here and returns, leaving its

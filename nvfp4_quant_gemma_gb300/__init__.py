@@ -16,5 +16,6 @@ from ._binding import (  # noqa: F401
     read_device_error,
     load,
     set_launch_policy,
+    set_pdl,
     status_string,
 )

@@ -49,6 +49,7 @@ def load() -> ctypes.CDLL:
             "add_rms_norm_quant": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "gnq_set_launch_policy": [I, I, I],
             "gnq_read_device_error": [P, I],
+            "gnq_set_pdl": [I],
             "gnq_quantize_fp8_values": [P, i64, P, P, P],
             "gnq_encode_e4m3_e2m1": [P, i64, P, P, P],
         }
@@ -65,7 +66,8 @@ def load() -> ctypes.CDLL:
 # Names the C ABI exports (checked by the test suite against include/gemma_nq.h).
 EXPORTS = ("gemma_add_rms_norm", "gemma_add_rms_norm_quant", "gemma_add_rms_norm_quant_parts",
            "add_rms_norm_quant", "gnq_status_string", "gnq_set_launch_policy",
-           "gnq_read_device_error", "gnq_encode_e4m3_e2m1", "gnq_quantize_fp8_values")
+           "gnq_read_device_error", "gnq_set_pdl", "gnq_encode_e4m3_e2m1",
+           "gnq_quantize_fp8_values")
 
 
 def status_string(status: int) -> str:
@@ -200,6 +202,11 @@ def set_launch_policy(kernel: int = 0, cluster: int = 0, vpt: int = 0) -> None:
     streaming kernel; cluster = CTAs per row; vpt = chunks per thread."""
     _check(load().gnq_set_launch_policy(int(kernel), int(cluster), int(vpt)),
            "gnq_set_launch_policy")
+
+
+def set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch on (default) or off for later calls."""
+    _check(load().gnq_set_pdl(1 if enable else 0), "gnq_set_pdl")
 
 
 def read_device_error(clear: bool = True) -> int:

@@ -39,6 +39,7 @@ DevInfo g_info[kMaxDevices];
 std::atomic<int> g_force_kernel{0};  // 0 auto, 1 row kernel, 2 streaming kernel
 std::atomic<int> g_force_cluster{0};
 std::atomic<int> g_force_vpt{0};
+std::atomic<int> g_pdl{1};  // 1: launch as programmatic dependents, 0: plain launches
 
 // Device properties and the error word's address, queried once per device
 // with that device current.
@@ -69,19 +70,23 @@ int granule(int mode) { return mode == MODE_NVFP4 ? 64 : mode == MODE_MXFP8 ? 32
 
 int max_threads(bool stream, int vpt) { return stream ? (vpt == 1 ? 1024 : 512) : 1024 / vpt; }
 
+// Elements one thread handles per unit (a whole NVFP4 block, else a chunk).
+int unit_elems(int mode) { return mode == MODE_NVFP4 ? 16 : 8; }
+
 bool row_shape_fits(int64_t H, int mode, int cluster, int vpt) {
     if (cluster < 1 || cluster > 8 || (cluster & (cluster - 1))) return false;
     if (vpt != 1 && vpt != 2 && vpt != 4) return false;
     if (H % ((int64_t)cluster * granule(mode)) != 0) return false;
-    const int64_t threads = (H / cluster / 8 + vpt - 1) / vpt;
+    const int64_t threads = (H / cluster / unit_elems(mode) + vpt - 1) / vpt;
     return threads <= max_threads(false, vpt);
 }
 
 // Streaming kernel shape: CTAs per SM and ring depth from the shared memory
 // a row needs (operands x 2H bytes per stage); false if it does not fit.
-bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int nops, int vpt, LaunchShape &ls) {
+bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops, int vpt,
+                  LaunchShape &ls) {
     if (vpt != 1 && vpt != 2 && vpt != 4) return false;
-    const int64_t threads = (H / 8 + vpt - 1) / vpt;
+    const int64_t threads = (H / unit_elems(mode) + vpt - 1) / vpt;
     if (threads > max_threads(true, vpt)) return false;
     const int64_t stage = (int64_t)nops * 2 * H;
     if (stage >= (1 << 20)) return false;  // mbarrier transaction count limit
@@ -99,6 +104,7 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int nops, int vpt, Lau
             ls.stages = (int)S;
             ls.smem = (size_t)(stage * S + 8 * S);
             ls.grid = M < (int64_t)d.sms * ctas ? M : (int64_t)d.sms * ctas;
+            ls.pdl = g_pdl.load() != 0;
             return true;
         }
     }
@@ -111,17 +117,18 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int nops, int vpt, Lau
 // CTA within 512 threads.
 LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops) {
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
-    LaunchShape ls{false, 1, 1, 32, M, 0, 0};
-    const int vpt_stream = H <= 4096 ? 1 : H <= 8192 ? 2 : 4;
+    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0};
+    const int64_t units = H / unit_elems(mode);
+    const int vpt_stream = units <= 512 ? 1 : units <= 1024 ? 2 : 4;
     const bool want_stream = fk == 2 || (fk == 0 && M >= 2LL * d.sms);
-    if (want_stream && stream_shape(d, M, H, nops, fv ? fv : vpt_stream, ls)) return ls;
-    if (want_stream && fv && stream_shape(d, M, H, nops, vpt_stream, ls)) return ls;
+    if (want_stream && stream_shape(d, M, H, mode, nops, fv ? fv : vpt_stream, ls)) return ls;
+    if (want_stream && fv && stream_shape(d, M, H, mode, nops, vpt_stream, ls)) return ls;
 
     while (ls.cluster < 8 && M * ls.cluster < 4LL * d.sms &&
            H % (2LL * ls.cluster * granule(mode)) == 0 && H / (2 * ls.cluster) >= 256)
         ls.cluster *= 2;
-    const int64_t nch = H / ls.cluster / 8;
-    while (ls.vpt < 4 && (nch + ls.vpt - 1) / ls.vpt > 512) ls.vpt *= 2;
+    const int64_t nunits = H / ls.cluster / unit_elems(mode);
+    while (ls.vpt < 4 && (nunits + ls.vpt - 1) / ls.vpt > 512) ls.vpt *= 2;
     if (fc || fv) {
         const int c = fc ? fc : ls.cluster, v = fv ? fv : ls.vpt;
         if (row_shape_fits(H, mode, c, v)) {
@@ -129,7 +136,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int n
             ls.vpt = v;
         }
     }
-    const int64_t threads = (H / ls.cluster / 8 + ls.vpt - 1) / ls.vpt;
+    const int64_t threads = (H / ls.cluster / unit_elems(mode) + ls.vpt - 1) / ls.vpt;
     ls.threads = (int)((threads + 31) / 32 * 32);
     ls.grid = M * ls.cluster;
     return ls;
@@ -187,6 +194,9 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
+    // Dependents may launch at once when this grid is resident in one wave
+    // (it cannot be starved of SMs by them); otherwise at its completion.
+    p.pdl_early = ls.pdl && (ls.stream || ls.grid * ls.threads <= 2048LL * d->sms / 2) ? 1 : 0;
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool parts = k > 1;
@@ -276,6 +286,12 @@ int gnq_set_launch_policy(int kernel, int cluster, int vpt) {
     gnq::g_force_kernel.store(kernel);
     gnq::g_force_cluster.store(cluster);
     gnq::g_force_vpt.store(vpt);
+    return GNQ_OK;
+}
+
+int gnq_set_pdl(int enable) {
+    if (enable != 0 && enable != 1) return GNQ_ERR_SHAPE;
+    gnq::g_pdl.store(enable);
     return GNQ_OK;
 }
 

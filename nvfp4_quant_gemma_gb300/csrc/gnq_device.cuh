@@ -34,6 +34,7 @@ struct Params {
     int seg;              // elements owned by one CTA (H / cluster size)
     int write_y;
     int stages;           // streaming kernel: rows in flight per CTA
+    int pdl_early;        // let dependent grids launch as soon as this one starts
     unsigned int *err;    // device error word
 };
 
@@ -253,6 +254,17 @@ __device__ __forceinline__ float div6(float amax) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Wait until the grid this one depends on has completed and its memory is
+// visible (returns at once when the launch was not programmatic).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the dependent grid to begin launching.
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // cluster helpers (distributed shared memory)
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_size() {
@@ -263,6 +275,11 @@ __device__ __forceinline__ uint32_t cluster_size() {
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
     return r;
 }
 __device__ __forceinline__ void cluster_arrive_release() {

@@ -9,7 +9,7 @@
 // with fp32 accumulation); MXFP8 per "vllm.model_executor.layers.
 // fused_allreduce_gemma_rms_norm", allreduce_gemma_rms_norm_mxfp8.
 //
-// Two kernels share one per-chunk epilogue (y, quantization, stores):
+// Two kernels share one per-unit epilogue (y, quantization, stores):
 //
 //   row_kernel     one CTA -- or a thread-block cluster of C CTAs meeting
 //                  through distributed shared memory -- per row, inputs
@@ -21,15 +21,18 @@
 //                  DRAM latency hides behind the arithmetic of earlier rows.
 //                  For large batches.
 //
-// Layout of work inside a CTA: each thread owns VPT 16-byte chunks (8
-// elements) of the row segment, chunk c = v * blockDim.x + threadIdx.x, so a
-// warp-wide access is one contiguous 512-byte line.  The sum of squares is an
-// fp32 warp shuffle tree plus one shared-memory stage that every thread adds
-// in the same order.  NVFP4: a 16-element block is two adjacent lanes (one
-// xor-shuffle for its amax); four consecutive blocks (8 lanes) have their
-// scale bytes adjacent in the swizzled layout, stored as one 32-bit word.
+// Work inside a CTA: a thread owns VPT units of U contiguous 16-byte chunks
+// (8U elements; U = 2 for NVFP4, so a thread holds whole 16-element blocks,
+// else U = 1), unit u = v * blockDim.x + threadIdx.x, so a warp-wide access
+// is one contiguous line.  Everything between the load and the stores stays
+// in registers.  The sum of squares is an fp32 warp shuffle tree, then a
+// second shuffle tree over the per-warp partials, the same in every warp.
 // Every rounding that decides a code is an IEEE round-to-nearest operation
 // (see gnq_device.cuh), so codes are exactly those of the fp32 reading.
+//
+// Both kernels wait on the preceding grid (programmatic dependent launch)
+// before their first global read, so they may be launched while it drains;
+// with `pdl_early` they also let their own dependents launch at once.
 #pragma once
 
 #include <type_traits>
@@ -37,6 +40,11 @@
 #include "gnq_device.cuh"
 
 namespace gnq {
+
+template <int MODE> struct Unit {
+    static constexpr int U = MODE == MODE_NVFP4 ? 2 : 1;  // chunks per unit
+    static constexpr int E = 8 * U;                        // elements per unit
+};
 
 // Per-CTA quantization constants.
 struct QuantCtx {
@@ -53,15 +61,33 @@ __device__ __forceinline__ void fill_es_table(float *tab, float g, int t, int nt
     }
 }
 
-// y for one chunk (8 values of y before rounding), then the quantizer and the
-// stores.  `t` is the thread index (lane groups for the scale gathers).
-// FAST selects the FP8 quotient path (uniform per CTA, see Fp8Div).
+__device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, float *es_smem,
+                                                   int t, int nt) {
+    QuantCtx qc;
+    qc.fd = make_fp8_div(1.f);
+    qc.g = 0.f;
+    qc.es_tab = es_smem;
+    if (mode == MODE_FP8) qc.fd = make_fp8_div(__ldg(p.scale));
+    if (mode == MODE_NVFP4) {
+        qc.g = __ldg(p.scale);
+        fill_es_table(es_smem, qc.g, t, nt);  // visible after the next __syncthreads
+    }
+    return qc;
+}
+
+// One unit of y (8U values before rounding): round, store y, quantize the
+// rounded values and store codes and scales.  `t` is the thread index.
 template <typename T, int MODE, bool FAST>
-__device__ __forceinline__ void epilogue_chunk(const Params &p, const QuantCtx &qc, float yf[8],
-                                               int64_t m, int64_t row, int col, bool ok, int t) {
-    const uint4 yb = pack8<T>(yf);
-    if (p.write_y && ok) st_v4(p.y + row + col, yb);
-    Act<T>::unpack(yb, yf);  // the rounded y feeds the quantizer
+__device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &qc,
+                                              float (&yf)[Unit<MODE>::E], int64_t m, int64_t row,
+                                              int col, bool ok, int t) {
+    constexpr int U = Unit<MODE>::U;
+#pragma unroll
+    for (int c = 0; c < U; ++c) {
+        const uint4 yb = pack8<T>(&yf[8 * c]);
+        if (p.write_y && ok) st_v4(p.y + row + col + 8 * c, yb);
+        Act<T>::unpack(yb, &yf[8 * c]);  // the rounded y feeds the quantizer
+    }
 
     if (MODE == MODE_FP8) {
         float d[8];
@@ -71,24 +97,21 @@ __device__ __forceinline__ void epilogue_chunk(const Params &p, const QuantCtx &
         const uint32_t hi = e4m3x4(d[4], d[5], d[6], d[7]);
         if (ok) st_v2(p.q + row + col, lo, hi);
     } else if (MODE == MODE_NVFP4) {
+        // one whole 16-element block per unit
         float amax = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yf[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));  // 16-element block
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(yf[i]));
         const float sf32 = __fmul_rn(qc.g, div6(amax));
         const uint32_t sf = e4m3x2(sf32, 0.f) & 0xFF;
         const float es = qc.es_tab[sf];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) yf[i] = __fmul_rn(yf[i], es);
-        const uint32_t codes = e2m1x8(yf);
-        if (ok) st_u32(p.q + ((row + col) >> 1), codes);
-        // scale bytes of 4 consecutive blocks (lanes 8i, 8i+2, 8i+4, 8i+6)
-        const uint32_t s1 = __shfl_down_sync(0xffffffffu, sf, 2);
-        const uint32_t s2 = __shfl_down_sync(0xffffffffu, sf, 4);
-        const uint32_t s3 = __shfl_down_sync(0xffffffffu, sf, 6);
-        if (ok && (t & 7) == 0) {
-            const uint32_t word = sf | (s1 << 8) | (s2 << 16) | (s3 << 24);
-            st_u32(p.block_scale + swizzled_group(m, col >> 4, p.Kp4), word);
+        for (int i = 0; i < 16; ++i) yf[i] = __fmul_rn(yf[i], es);
+        const uint32_t lo = e2m1x8(&yf[0]);
+        const uint32_t hi = e2m1x8(&yf[8]);
+        if (ok) {
+            st_v2(p.q + ((row + col) >> 1), lo, hi);
+            const int b = col >> 4;
+            st_u8(p.block_scale + swizzled_group(m, b & ~3, p.Kp4) + (b & 3), sf);
         }
     } else if (MODE == MODE_MXFP8) {
         float amax = 0.f;
@@ -122,109 +145,126 @@ __device__ __forceinline__ float inv_rms(const Params &p, float tot) {
     return rsqrtf(__fadd_rn(__fmul_rn(tot, p.inv_h), p.eps));
 }
 
-__device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, float *es_smem,
-                                                   int t, int nt) {
-    QuantCtx qc;
-    qc.fd = make_fp8_div(1.f);
-    qc.g = 0.f;
-    qc.es_tab = es_smem;
-    if (mode == MODE_FP8) qc.fd = make_fp8_div(__ldg(p.scale));
-    if (mode == MODE_NVFP4) {
-        qc.g = __ldg(p.scale);
-        fill_es_table(es_smem, qc.g, t, nt);  // visible after the next __syncthreads
-    }
-    return qc;
-}
-
 // ---------------------------------------------------------------------------
 // row_kernel: one CTA (or cluster) per row, inputs straight to registers
 // ---------------------------------------------------------------------------
 template <typename T, int MODE, bool PARTS, int VPT>
 __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
+    constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     __shared__ float warp_ss[32];
     __shared__ float cta_ss;
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
     const uint32_t C = cluster_size();
     const uint32_t rank = C > 1 ? cluster_rank() : 0;
-    const int64_t m = blockIdx.x / C;
+    const int64_t m = C > 1 ? (int64_t)cluster_id_x() : (int64_t)blockIdx.x;
     const int NT = blockDim.x;
     const int t = threadIdx.x;
-    const int nch = p.seg >> 3;
+    const int nunits = p.seg / E;
     const int64_t row = m * (int64_t)p.H;
 
     int col[VPT];
     bool ok[VPT];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-        const int c = v * NT + t;
-        ok[v] = c < nch;
-        col[v] = (int)rank * p.seg + c * 8;
+        const int u = v * NT + t;
+        ok[v] = u < nunits;
+        col[v] = (int)rank * p.seg + u * E;
     }
 
+    pdl_wait();  // inputs may come from the preceding grid
+    if (p.pdl_early) pdl_trigger();
+
     // ---- issue every load of the row segment up front ----
-    uint4 rv[VPT], xv[VPT], wv[VPT];
+    uint4 rv[VPT][U], xv[VPT][U], wv[VPT][U];
     const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        rv[v] = (p.residual && ok[v]) ? ld_inout(p.residual + row + col[v]) : zero;
-        xv[v] = ok[v] ? ld_stream(p.x + row + col[v]) : zero;
-    }
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int c = 0; c < U; ++c) {
+            rv[v][c] = (p.residual && ok[v]) ? ld_inout(p.residual + row + col[v] + 8 * c) : zero;
+            xv[v][c] = ok[v] ? ld_stream(p.x + row + col[v] + 8 * c) : zero;
+        }
     if (PARTS) {
         // a = dtype(((p0 + p1) + p2) + ...), fp32 accumulation in index order.
         // Partials are fetched four at a time so their loads are in flight
         // together; the adds still run strictly in index order.
-        float acc[VPT][8];
+        float acc[VPT][E];
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) Act<T>::unpack(xv[v], acc[v]);
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+            for (int c = 0; c < U; ++c) Act<T>::unpack(xv[v][c], &acc[v][8 * c]);
         for (int p0 = 1; p0 < p.k; p0 += 4) {
-            uint4 pv[4][VPT];
+            uint4 pv[4][VPT][U];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint16_t *xp = p.x + (p0 + j) * p.part_stride + row;
 #pragma unroll
                 for (int v = 0; v < VPT; ++v)
-                    pv[j][v] = (p0 + j < p.k && ok[v]) ? ld_stream(xp + col[v]) : zero;
+#pragma unroll
+                    for (int c = 0; c < U; ++c)
+                        pv[j][v][c] = (p0 + j < p.k && ok[v]) ? ld_stream(xp + col[v] + 8 * c) : zero;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 if (p0 + j < p.k) {
 #pragma unroll
-                    for (int v = 0; v < VPT; ++v) {
-                        float f[8];
-                        Act<T>::unpack(pv[j][v], f);
+                    for (int v = 0; v < VPT; ++v)
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) acc[v][i] = __fadd_rn(acc[v][i], f[i]);
-                    }
+                        for (int c = 0; c < U; ++c) {
+                            float f[8];
+                            Act<T>::unpack(pv[j][v][c], f);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                acc[v][8 * c + i] = __fadd_rn(acc[v][8 * c + i], f[i]);
+                        }
                 }
             }
         }
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) xv[v] = pack8<T>(acc[v]);
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+            for (int c = 0; c < U; ++c) xv[v][c] = pack8<T>(&acc[v][8 * c]);
     }
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) wv[v] = ok[v] ? ld_weight(p.w + col[v]) : zero;
+    for (int v = 0; v < VPT; ++v)
+#pragma unroll
+        for (int c = 0; c < U; ++c) wv[v][c] = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : zero;
 
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
-    // ---- h = dtype(a + residual), residual <- h, sum of squares ----
-    float h[VPT][8];
+    // ---- h = dtype(a + residual), sum of squares ----
+    float h[VPT][E];
     float ss = 0.f;
 #pragma unroll
-    for (int v = 0; v < VPT; ++v) {
-        Act<T>::unpack(xv[v], h[v]);
-        if (p.residual) {
-            float r[8];
-            Act<T>::unpack(rv[v], r);
+    for (int v = 0; v < VPT; ++v)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) r[i] = __fadd_rn(h[v][i], r[i]);
-            const uint4 hb = pack8<T>(r);
-            if (ok[v]) st_v4(p.residual + row + col[v], hb);
-            Act<T>::unpack(hb, h[v]);
+        for (int c = 0; c < U; ++c) {
+            Act<T>::unpack(xv[v][c], &h[v][8 * c]);
+            if (p.residual) {
+                float r[8];
+                Act<T>::unpack(rv[v][c], r);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[i] = __fadd_rn(h[v][8 * c + i], r[i]);
+                rv[v][c] = pack8<T>(r);  // the new residual, stored below
+                Act<T>::unpack(rv[v][c], &h[v][8 * c]);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) ss = fmaf(h[v][8 * c + i], h[v][8 * c + i], ss);
         }
+    // A CTA outside a cluster stores the residual now; in a cluster it waits
+    // until after the cluster barrier, whose release would otherwise have to
+    // wait for these stores.
+    auto store_residual = [&]() {
+        if (p.residual) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) ss = fmaf(h[v][i], h[v][i], ss);
-    }
+            for (int v = 0; v < VPT; ++v)
+#pragma unroll
+                for (int c = 0; c < U; ++c)
+                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, rv[v][c]);
+        }
+    };
+    if (C == 1) store_residual();
 
     // ---- row reduction: warps, then CTA, then cluster ----
     ss = warp_sum(ss);
@@ -238,6 +278,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
         tot = 0.f;
         for (uint32_t r = 0; r < C; ++r) tot += ld_peer_f32(&cta_ss, r);
         cluster_arrive_relaxed();  // this CTA's reads of its peers are done
+        store_residual();
     }
     const float inv = inv_rms(p, tot);
 
@@ -245,12 +286,17 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     auto finish = [&](auto fast) {
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
-            float wf[8], yf[8];
-            Act<T>::unpack(wv[v], wf);
+            float yf[E];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-                yf[i] = __fmul_rn(__fmul_rn(h[v][i], inv), __fadd_rn(p.weight_bias, wf[i]));
-            epilogue_chunk<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+            for (int c = 0; c < U; ++c) {
+                float wf[8];
+                Act<T>::unpack(wv[v][c], wf);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    yf[8 * c + i] = __fmul_rn(__fmul_rn(h[v][8 * c + i], inv),
+                                              __fadd_rn(p.weight_bias, wf[i]));
+            }
+            epilogue_unit<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
         }
     };
     if (MODE != MODE_FP8 || qc.fd.fast) finish(std::true_type{});
@@ -266,6 +312,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 // per stage.  Operands of a row: partial 0..k-1, then the residual.
 template <typename T, int MODE, bool PARTS, int VPT>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
+    constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     extern __shared__ __align__(128) uint8_t dsmem[];
     __shared__ float warp_ss[2][32];
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
@@ -281,11 +328,11 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
     const uint32_t bars = base + stage_bytes * S;  // 8-byte aligned: row_bytes % 16 == 0
 
     // rows of this CTA: m_i = blockIdx.x + i * G, i < n_rows
-    const int64_t n_rows = p.M > blockIdx.x ? (p.M - 1 - blockIdx.x) / G + 1 : 0;
+    const int n_rows = p.M > blockIdx.x ? (int)((p.M - 1 - blockIdx.x) / G + 1) : 0;
 
-    auto issue = [&](int64_t i) {  // thread 0: start the loads of local row i
-        const int s = (int)(i % S);
-        const int64_t m = blockIdx.x + i * G;
+    // thread 0: start the loads of local row i into stage s
+    auto issue = [&](int i, int s) {
+        const int64_t m = blockIdx.x + (int64_t)i * G;
         const uint32_t bar = bars + 8u * s;
         const uint32_t dst = base + stage_bytes * s;
         mbar_expect_tx(bar, stage_bytes);
@@ -294,34 +341,40 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         if (p.residual) bulk_g2s(dst + row_bytes * p.k, p.residual + m * p.H, row_bytes, bar);
     };
 
+    pdl_wait();  // inputs may come from the preceding grid
+    if (p.pdl_early) pdl_trigger();
+
     if (t == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int64_t i = 0; i < n_rows && i < S; ++i) issue(i);
+        for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
     }
 
     // per-CTA constants: (bias + w) in fp32, quantizer context
     int col[VPT];
     bool ok[VPT];
-    float bw[VPT][8];
-    const int nch = p.H >> 3;
+    float bw[VPT][E];
+    const int nunits = p.H / E;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
-        const int c = v * NT + t;
-        ok[v] = c < nch;
-        col[v] = c * 8;
-        const uint4 wv = ok[v] ? ld_weight(p.w + col[v]) : make_uint4(0, 0, 0, 0);
-        Act<T>::unpack(wv, bw[v]);
+        const int u = v * NT + t;
+        ok[v] = u < nunits;
+        col[v] = u * E;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) bw[v][i] = __fadd_rn(p.weight_bias, bw[v][i]);
+        for (int c = 0; c < U; ++c) {
+            const uint4 wv = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
+            Act<T>::unpack(wv, &bw[v][8 * c]);
+        }
+#pragma unroll
+        for (int i = 0; i < E; ++i) bw[v][i] = __fadd_rn(p.weight_bias, bw[v][i]);
     }
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
     __syncthreads();  // barriers initialised, table filled
 
-    for (int64_t i = 0; i < n_rows; ++i) {
-        const int s = (int)(i % S);
-        const uint32_t parity = (uint32_t)((i / S) & 1);
-        const int64_t m = blockIdx.x + i * G;
+    int s = 0;            // stage of row i (i mod S)
+    uint32_t parity = 0;  // phase parity of that stage's barrier ((i / S) mod 2)
+    for (int i = 0; i < n_rows; ++i) {
+        const int64_t m = blockIdx.x + (int64_t)i * G;
         const int64_t row = m * (int64_t)p.H;
         const uint32_t stage = base + stage_bytes * s;
 
@@ -331,66 +384,81 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
             // flight land (bounded again) before the shared memory goes away.
             if (t == 0) {
                 atomicOr(p.err, (unsigned)DEVERR_WAIT_TIMEOUT);
-                for (int64_t j = i; j < n_rows && j < i + S; ++j)
-                    mbar_wait_bounded(bars + 8u * (int)(j % S), (uint32_t)((j / S) & 1));
+                int sj = s;
+                uint32_t pj = parity;
+                for (int j = i; j < n_rows && j < i + S; ++j) {
+                    mbar_wait_bounded(bars + 8u * sj, pj);
+                    if (++sj == S) {
+                        sj = 0;
+                        pj ^= 1u;
+                    }
+                }
             }
             __syncthreads();
             return;
         }
 
         // ---- a = sum of partials (fp32, index order), h = dtype(a + r) ----
-        float h[VPT][8];
+        float h[VPT][E];
         float ss = 0.f;
 #pragma unroll
-        for (int v = 0; v < VPT; ++v) {
-            const uint32_t off = (uint32_t)col[v] * 2u;
-            uint4 xv = ok[v] ? lds_v4(stage + off) : make_uint4(0, 0, 0, 0);
-            if (PARTS) {
-                float acc[8];
-                Act<T>::unpack(xv, acc);
-                for (int op = 1; op < p.k; ++op) {
-                    float f[8];
-                    Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * op + off)
-                                         : make_uint4(0, 0, 0, 0), f);
+        for (int v = 0; v < VPT; ++v)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+            for (int c = 0; c < U; ++c) {
+                const uint32_t off = (uint32_t)(col[v] + 8 * c) * 2u;
+                uint4 xv = ok[v] ? lds_v4(stage + off) : make_uint4(0, 0, 0, 0);
+                if (PARTS) {
+                    float acc[8];
+                    Act<T>::unpack(xv, acc);
+                    for (int op = 1; op < p.k; ++op) {
+                        float f[8];
+                        Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * op + off)
+                                             : make_uint4(0, 0, 0, 0), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+                    }
+                    xv = pack8<T>(acc);
                 }
-                xv = pack8<T>(acc);
-            }
-            Act<T>::unpack(xv, h[v]);
-            if (p.residual) {
-                float r[8];
-                Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * p.k + off) : make_uint4(0, 0, 0, 0), r);
+                float *hc = &h[v][8 * c];
+                Act<T>::unpack(xv, hc);
+                if (p.residual) {
+                    float r[8];
+                    Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * p.k + off)
+                                         : make_uint4(0, 0, 0, 0), r);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) r[e] = __fadd_rn(h[v][e], r[e]);
-                const uint4 hb = pack8<T>(r);
-                if (ok[v]) st_v4(p.residual + row + col[v], hb);
-                Act<T>::unpack(hb, h[v]);
-            }
+                    for (int e = 0; e < 8; ++e) r[e] = __fadd_rn(hc[e], r[e]);
+                    const uint4 hb = pack8<T>(r);
+                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, hb);
+                    Act<T>::unpack(hb, hc);
+                }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ss = fmaf(h[v][e], h[v][e], ss);
-        }
+                for (int e = 0; e < 8; ++e) ss = fmaf(hc[e], hc[e], ss);
+            }
 
         ss = warp_sum(ss);
         if ((t & 31) == 0) warp_ss[i & 1][t >> 5] = ss;
         __syncthreads();  // also: every thread is done reading this stage
         if (t == 0 && i + S < n_rows) {
             fence_async_shared();
-            issue(i + S);
+            issue(i + S, s);
         }
         const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
 
         auto finish = [&](auto fast) {
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
-                float yf[8];
+                float yf[E];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) yf[e] = __fmul_rn(__fmul_rn(h[v][e], inv), bw[v][e]);
-                epilogue_chunk<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+                for (int e = 0; e < E; ++e) yf[e] = __fmul_rn(__fmul_rn(h[v][e], inv), bw[v][e]);
+                epilogue_unit<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
             }
         };
         if (MODE != MODE_FP8 || qc.fd.fast) finish(std::true_type{});
         else finish(std::false_type{});
+        if (++s == S) {
+            s = 0;
+            parity ^= 1u;
+        }
     }
 }
 

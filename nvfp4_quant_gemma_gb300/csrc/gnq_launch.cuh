@@ -17,6 +17,7 @@ struct LaunchShape {
     int64_t grid;    // CTAs
     int stages;      // streaming kernel: rows in flight per CTA
     size_t smem;     // streaming kernel: dynamic shared memory bytes
+    bool pdl;        // launch as a programmatic dependent of the preceding grid
 };
 
 template <int MODE>
@@ -50,15 +51,21 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
     cfg.blockDim = dim3((unsigned)ls.threads, 1, 1);
     cfg.dynamicSmemBytes = ls.stream ? ls.smem : 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
     if (!ls.stream && ls.cluster > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)ls.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.numAttrs = 1;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)ls.cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
     }
+    if (ls.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.numAttrs = n;
     cfg.attrs = attr;
     return cudaLaunchKernelEx(&cfg, fn, p);
 }

@@ -353,6 +353,44 @@ def test_stream_and_graph_capture(gnq):
         assert torch.equal(yy, y1) and torch.equal(rr, r1)
 
 
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0)])
+def test_pdl_on_and_off_agree(gnq, mode, scale):
+    """Programmatic dependent launch changes launch timing only: a chain of
+    dependent calls (each consuming the previous residual) gives the same
+    bits with it on and off, eagerly and in a captured graph."""
+    dev = torch.device("cuda")
+    x, r, w = _make(256, 4096, "bf16", seed=31)
+    xd, wd = x.to(dev), w.to(dev)
+    sd = torch.tensor([scale], device=dev)
+
+    def chain(pdl, graph):
+        gnq.set_pdl(pdl)
+        try:
+            rd = r.to(dev)
+            outs = [gnq.alloc_outputs(256, 4096, mode, True, xd) for _ in range(4)]
+            def run():
+                for o in outs:  # each call reads the residual the previous one wrote
+                    gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    run()
+                rd.copy_(r.to(dev))
+                g.replay()
+            else:
+                run()
+            torch.cuda.synchronize()
+            return [rd.clone()] + [t.view(torch.uint8).clone() if t.dtype != torch.bfloat16 else t.clone()
+                                   for o in outs for t in o if t is not None]
+        finally:
+            gnq.set_pdl(True)
+
+    ref = chain(False, False)
+    for pdl, graph in ((True, False), (True, True), (False, True)):
+        got = chain(pdl, graph)
+        assert all(torch.equal(a, b) for a, b in zip(ref, got))
+
+
 def test_status_codes_with_device_buffers(gnq):
     lib = gnq.load()
     import ctypes
