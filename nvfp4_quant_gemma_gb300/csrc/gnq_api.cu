@@ -111,24 +111,38 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops, in
     return false;
 }
 
-// Launch shape.  Large batches (M >= 2 x SMs) stream rows through persistent
-// CTAs; smaller ones give each row a CTA, split over a cluster while the grid
-// would otherwise have fewer than ~4 CTAs per SM.  Chunks per thread keep a
-// CTA within 512 threads.
-LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops) {
+// Automatic launch shape, from sweeps of every kernel / cluster / chunks-per-
+// thread combination on the decode, prefill and partial-sum workloads:
+//   * M < 16 x SMs (decode batches, mid-size prefill): one CTA per row,
+//     one unit per thread; the row is split over a cluster only when there
+//     are very few rows and they are wide (M x C < 32, >= 2048 elements per
+//     CTA), where the extra SMs outweigh the cluster barrier.
+//   * larger M: rows stream through persistent CTAs of ~256 threads, except
+//     FP8 / MXFP8 / no-quant with a residual and no partials, where a CTA per
+//     row with four units per thread keeps the most loads in flight.
+LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int k, bool res) {
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
+    const int nops = k + (res ? 1 : 0);
     LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0};
     const int64_t units = H / unit_elems(mode);
-    const int vpt_stream = units <= 512 ? 1 : units <= 1024 ? 2 : 4;
-    const bool want_stream = fk == 2 || (fk == 0 && M >= 2LL * d.sms);
+    int vpt_stream = 1;
+    while (vpt_stream < 4 && (units + vpt_stream - 1) / vpt_stream > 256) vpt_stream *= 2;
+    const bool big = M >= 16LL * d.sms;
+    const bool row_big = big && k == 1 && res && mode != MODE_NVFP4;
+    const bool want_stream = fk == 2 || (fk == 0 && big && !row_big);
     if (want_stream && stream_shape(d, M, H, mode, nops, fv ? fv : vpt_stream, ls)) return ls;
     if (want_stream && fv && stream_shape(d, M, H, mode, nops, vpt_stream, ls)) return ls;
 
-    while (ls.cluster < 8 && M * ls.cluster < 4LL * d.sms &&
-           H % (2LL * ls.cluster * granule(mode)) == 0 && H / (2 * ls.cluster) >= 256)
+    if (fk == 0 && row_big) ls.vpt = 4;
+    const int64_t gran2 = 2LL * granule(mode);
+    while (ls.cluster < 8 && M * ls.cluster < 32 && H % (gran2 * ls.cluster) == 0 &&
+           H / (2 * ls.cluster) >= 2048)
+        ls.cluster *= 2;
+    // wide rows: a CTA handles at most 1024 units
+    while (ls.cluster < 8 && units / ls.cluster > 1024 && H % (gran2 * ls.cluster) == 0)
         ls.cluster *= 2;
     const int64_t nunits = H / ls.cluster / unit_elems(mode);
-    while (ls.vpt < 4 && (nunits + ls.vpt - 1) / ls.vpt > 512) ls.vpt *= 2;
+    while (ls.vpt < 4 && (nunits + ls.vpt - 1) / ls.vpt > max_threads(false, ls.vpt)) ls.vpt *= 2;
     if (fc || fv) {
         const int c = fc ? fc : ls.cluster, v = fv ? fv : ls.vpt;
         if (row_shape_fits(H, mode, c, v)) {
@@ -190,7 +204,7 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 
     const DevInfo *d = dev_info();
     if (!d) return GNQ_ERR_CUDA;
-    const LaunchShape ls = choose_shape(*d, M, H, mode, k + (residual ? 1 : 0));
+    const LaunchShape ls = choose_shape(*d, M, H, mode, k, residual != nullptr);
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
