@@ -224,12 +224,35 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     return e == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
 }
 
+// Groups of 8 values through the kernels' FP8 encoder, on the path a kernel
+// would take: pairs when every y * (1/s) of the group is finite, else the
+// clamped form (IEEE division for extreme scales); a ragged tail goes
+// through the single-value form.
 __global__ void fp8_values_kernel(const float *y, int64_t n, const float *scale, uint8_t *q) {
     const Fp8Div fd = make_fp8_div(*scale);
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
-         i += (int64_t)gridDim.x * blockDim.x) {
-        const float d = fd.fast ? fp8_quotient<true>(y[i], fd) : fp8_quotient<false>(y[i], fd);
-        q[i] = (uint8_t)(e4m3x2(d, 0.f) & 0xFF);
+    const int64_t groups = n / 8;
+    for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
+         g += (int64_t)gridDim.x * blockDim.x) {
+        float v[8];
+        bool pair_ok = true;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = y[8 * g + i];
+            pair_ok = pair_ok && fabsf(v[i]) * fabsf(fd.r) < 0x1p126f;
+        }
+        uint32_t lo, hi;
+        if (!fd.fast) fp8_codes8<FP8_IEEE>(v, fd, lo, hi);
+        else if (pair_ok) fp8_codes8<FP8_PAIR>(v, fd, lo, hi);
+        else fp8_codes8<FP8_CLAMP>(v, fd, lo, hi);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[8 * g + i] = (uint8_t)(lo >> (8 * i));
+            q[8 * g + 4 + i] = (uint8_t)(hi >> (8 * i));
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
+        const int64_t i = groups * 8 + threadIdx.x;
+        q[i] = (uint8_t)(e4m3x2(fp8_quotient(y[i], fd), 0.f) & 0xFF);
     }
 }
 
@@ -335,7 +358,8 @@ int gnq_quantize_fp8_values(const float *y, int64_t n, const float *scale, uint8
     if (n < 0) return GNQ_ERR_SHAPE;
     if (n == 0) return GNQ_OK;
     if (!y || !scale || !q) return GNQ_ERR_NULL;
-    const int64_t blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    const int64_t groups = n / 8 + 1;
+    const int64_t blocks = (groups + 255) / 256 < 4096 ? (groups + 255) / 256 : 4096;
     gnq::fp8_values_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         y, n, scale, q);
     return cudaGetLastError() == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;

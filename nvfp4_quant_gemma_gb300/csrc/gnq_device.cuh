@@ -209,13 +209,59 @@ __device__ __forceinline__ float div_fma(float a, float b, float r, float &q0) {
     return __fmaf_rn(rem, r, q0);
 }
 
-// The static FP8 quotient y / s as the E4M3 encoder needs it.  `fast` holds
-// for 2^-80 <= s <= 2^80 (s positive): then |y| is first clamped to
-// ylim = 1024 s (a clamped quotient is >= 1024 and saturates to 448, like
-// the true one; NaN passes through), the quotient of |y| is taken with the
-// FMA correction (exact for |y| >= 2^-103; below that |y/s| < 2^-23, a zero
-// code either way), and the sign of y is put back -- which also gives -0 for
-// y = -0.  Other scales take the IEEE division.
+// ---------------------------------------------------------------------------
+// paired fp32 arithmetic (Blackwell f32x2: two IEEE round-to-nearest lanes)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+// In-place element-wise helpers on arrays of n (even) floats.
+template <int N> __device__ __forceinline__ void mul_arr(float (&v)[N], const float *w) {
+#pragma unroll
+    for (int i = 0; i < N; i += 2) upk2(mul2(pk2(v[i], v[i + 1]), pk2(w[i], w[i + 1])), v[i], v[i + 1]);
+}
+template <int N> __device__ __forceinline__ void mul_arr_s(float *v, float c) {
+    const uint64_t cc = pk2(c, c);
+#pragma unroll
+    for (int i = 0; i < N; i += 2) upk2(mul2(pk2(v[i], v[i + 1]), cc), v[i], v[i + 1]);
+}
+
+// The static FP8 quotient y / s as the E4M3 encoder needs it.  Three paths,
+// chosen once per CTA:
+//   FP8_PAIR  (2^-80 <= s <= 2^80 and y * (1/s) provably finite): the
+//             correction step on pairs, in negated form:
+//             n0 = RN(y * -r), rem = y + n0 * s (exact), n1 = RN(rem * -r + n0)
+//             = -RN(y / s) for every y, signed zeros included; the caller
+//             flips the sign bits of the codes.
+//   FP8_CLAMP (2^-80 <= s <= 2^80): |y| first clamped to ylim = 1024 s (a
+//             clamped quotient is >= 1024 and saturates to 448 like the true
+//             one; NaN passes through), the correction step on |y|, the sign
+//             of y put back.
+//   FP8_IEEE  other scales: IEEE division.
+// The correction is exact for |y| >= 2^-103; below that |y/s| < 2^-23, a
+// zero code of the right sign either way.
+enum { FP8_IEEE = 0, FP8_CLAMP = 1, FP8_PAIR = 2 };
+
 struct Fp8Div {
     float s, r, ylim;
     bool fast;
@@ -236,13 +282,44 @@ __device__ __forceinline__ float min_nan(float a, float b) {
     return d;
 }
 
-template <bool FAST>
+// Eight E4M3 codes of y[0..8) / s (FP8_PAIR: of -(y / s), see above) as two words.
+template <int PATH>
+__device__ __forceinline__ void fp8_codes8(const float *y, const Fp8Div &d, uint32_t &lo,
+                                           uint32_t &hi) {
+    float q[8];
+    if (PATH == FP8_PAIR) {
+        const uint64_t nr = pk2(-d.r, -d.r), s2 = pk2(d.s, d.s);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const uint64_t y2 = pk2(y[i], y[i + 1]);
+            const uint64_t n0 = mul2(y2, nr);
+            const uint64_t rem = fma2(n0, s2, y2);
+            upk2(fma2(rem, nr, n0), q[i], q[i + 1]);
+        }
+        lo = e4m3x4(q[0], q[1], q[2], q[3]) ^ 0x80808080u;
+        hi = e4m3x4(q[4], q[5], q[6], q[7]) ^ 0x80808080u;
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (PATH == FP8_IEEE) {
+            q[i] = __fdiv_rn(y[i], d.s);
+        } else {
+            const float a = min_nan(fabsf(y[i]), d.ylim);
+            float q0;
+            q[i] = copysignf(div_fma(a, d.s, d.r, q0), y[i]);
+        }
+    }
+    lo = e4m3x4(q[0], q[1], q[2], q[3]);
+    hi = e4m3x4(q[4], q[5], q[6], q[7]);
+}
+
+// Single value, for the diagnostic entry point (FP8_CLAMP or FP8_IEEE).
 __device__ __forceinline__ float fp8_quotient(float y, const Fp8Div &d) {
-    if (!FAST) return __fdiv_rn(y, d.s);
+    if (!d.fast) return __fdiv_rn(y, d.s);
     const float a = min_nan(fabsf(y), d.ylim);
     float q0;
-    const float q = div_fma(a, d.s, d.r, q0);
-    return copysignf(q, y);
+    return copysignf(div_fma(a, d.s, d.r, q0), y);
 }
 
 // amax / 6 correctly rounded (amax >= 0).

@@ -76,8 +76,9 @@ __device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, fl
 }
 
 // One unit of y (8U values before rounding): round, store y, quantize the
-// rounded values and store codes and scales.  `t` is the thread index.
-template <typename T, int MODE, bool FAST>
+// rounded values and store codes and scales.  `t` is the thread index;
+// FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA.
+template <typename T, int MODE, int FP8PATH>
 __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &qc,
                                               float (&yf)[Unit<MODE>::E], int64_t m, int64_t row,
                                               int col, bool ok, int t) {
@@ -90,11 +91,8 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
     }
 
     if (MODE == MODE_FP8) {
-        float d[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d[i] = fp8_quotient<FAST>(yf[i], qc.fd);
-        const uint32_t lo = e4m3x4(d[0], d[1], d[2], d[3]);
-        const uint32_t hi = e4m3x4(d[4], d[5], d[6], d[7]);
+        uint32_t lo, hi;
+        fp8_codes8<FP8PATH>(yf, qc.fd, lo, hi);
         if (ok) st_v2(p.q + row + col, lo, hi);
     } else if (MODE == MODE_NVFP4) {
         // one whole 16-element block per unit
@@ -103,9 +101,7 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(yf[i]));
         const float sf32 = __fmul_rn(qc.g, div6(amax));
         const uint32_t sf = e4m3x2(sf32, 0.f) & 0xFF;
-        const float es = qc.es_tab[sf];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) yf[i] = __fmul_rn(yf[i], es);
+        mul_arr_s<16>(yf, qc.es_tab[sf]);
         const uint32_t lo = e2m1x8(&yf[0]);
         const uint32_t hi = e2m1x8(&yf[8]);
         if (ok) {
@@ -121,12 +117,9 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));  // 32-element block
         int code = 0;
         if (amax > 0.f) code = min(max(ilogbf(amax) - 8 + 127, 0), 254);
-        const float inv_x = ldexpf(1.0f, 127 - code);  // 1 / 2^(code-127), exact
-        float d[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) d[i] = __fmul_rn(yf[i], inv_x);
-        const uint32_t lo = e4m3x4(d[0], d[1], d[2], d[3]);
-        const uint32_t hi = e4m3x4(d[4], d[5], d[6], d[7]);
+        mul_arr_s<8>(yf, ldexpf(1.0f, 127 - code));  // y / 2^(code-127), exact
+        const uint32_t lo = e4m3x4(yf[0], yf[1], yf[2], yf[3]);
+        const uint32_t hi = e4m3x4(yf[4], yf[5], yf[6], yf[7]);
         if (ok) st_v2(p.q + row + col, lo, hi);
         if (ok && (t & 3) == 0)
             st_u8(p.block_scale + m * (int64_t)(p.H >> 5) + (col >> 5), (uint32_t)code);
@@ -235,23 +228,34 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 
     // ---- h = dtype(a + residual), sum of squares ----
     float h[VPT][E];
-    float ss = 0.f;
+    uint64_t ss2 = 0;  // two fp32 partial sums (+0, +0)
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int c = 0; c < U; ++c) {
-            Act<T>::unpack(xv[v][c], &h[v][8 * c]);
+            float *hc = &h[v][8 * c];
+            Act<T>::unpack(xv[v][c], hc);
             if (p.residual) {
                 float r[8];
                 Act<T>::unpack(rv[v][c], r);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) r[i] = __fadd_rn(h[v][8 * c + i], r[i]);
+                for (int i = 0; i < 8; i += 2)
+                    upk2(add2(pk2(hc[i], hc[i + 1]), pk2(r[i], r[i + 1])), r[i], r[i + 1]);
                 rv[v][c] = pack8<T>(r);  // the new residual, stored below
-                Act<T>::unpack(rv[v][c], &h[v][8 * c]);
+                Act<T>::unpack(rv[v][c], hc);
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) ss = fmaf(h[v][8 * c + i], h[v][8 * c + i], ss);
+            for (int i = 0; i < 8; i += 2) {
+                const uint64_t h2 = pk2(hc[i], hc[i + 1]);
+                ss2 = fma2(h2, h2, ss2);
+            }
         }
+    float ss;
+    {
+        float a, b;
+        upk2(ss2, a, b);
+        ss = a + b;
+    }
     // A CTA outside a cluster stores the residual now; in a cluster it waits
     // until after the cluster barrier, whose release would otherwise have to
     // wait for these stores.
@@ -283,7 +287,8 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     const float inv = inv_rms(p, tot);
 
     // ---- y = dtype(h * inv * (bias + w)), then quantize the rounded y ----
-    auto finish = [&](auto fast) {
+    auto finish = [&](auto path) {
+        const uint64_t inv2 = pk2(inv, inv), bias2 = pk2(p.weight_bias, p.weight_bias);
 #pragma unroll
         for (int v = 0; v < VPT; ++v) {
             float yf[E];
@@ -292,15 +297,21 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
                 float wf[8];
                 Act<T>::unpack(wv[v][c], wf);
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    yf[8 * c + i] = __fmul_rn(__fmul_rn(h[v][8 * c + i], inv),
-                                              __fadd_rn(p.weight_bias, wf[i]));
+                for (int i = 0; i < 8; i += 2) {
+                    const uint64_t bw2 = add2(bias2, pk2(wf[i], wf[i + 1]));
+                    const uint64_t hi2 = mul2(pk2(h[v][8 * c + i], h[v][8 * c + i + 1]), inv2);
+                    upk2(mul2(hi2, bw2), yf[8 * c + i], yf[8 * c + i + 1]);
+                }
             }
-            epilogue_unit<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+            epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, m, row, col[v], ok[v], t);
         }
     };
-    if (MODE != MODE_FP8 || qc.fd.fast) finish(std::true_type{});
-    else finish(std::false_type{});
+    // FP8 quotient path: pairs when y * (1/s) cannot overflow (fp16 y is
+    // at most 65504 and |1/s| <= 2^80), else the clamped form.
+    if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
+    else if (MODE == MODE_FP8 && !std::is_same<T, __half>::value)
+        finish(std::integral_constant<int, FP8_CLAMP>{});
+    else finish(std::integral_constant<int, FP8_PAIR>{});
 
     if (C > 1) cluster_wait();  // peers may still be reading this CTA's partial
 }
@@ -369,7 +380,30 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         for (int i = 0; i < E; ++i) bw[v][i] = __fadd_rn(p.weight_bias, bw[v][i]);
     }
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
-    __syncthreads();  // barriers initialised, table filled
+
+    // FP8 quotient path for this CTA.  Pairs need y * (1/s) finite: fp16 y is
+    // at most 65504; for bf16, |y_j| <= sqrt(H) |bias + w_j| (1 + 2^-8) since
+    // |h_j| / rms(h) <= sqrt(H) when eps >= 0, so a bound on max |bias + w|
+    // decides it.
+    int fp8_path = FP8_PAIR;
+    if (MODE == MODE_FP8) {
+        float wmax = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+            for (int i = 0; i < E; ++i) wmax = fmaxf(wmax, fabsf(bw[v][i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+        if ((t & 31) == 0) warp_ss[1][t >> 5] = wmax;
+        __syncthreads();
+        float all = (t & 31) < (NT >> 5) ? warp_ss[1][t & 31] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) all = fmaxf(all, __shfl_xor_sync(0xffffffffu, all, o));
+        const float bound = sqrtf((float)p.H) * all * 1.01f * fabsf(qc.fd.r);
+        const bool pair_ok = std::is_same<T, __half>::value || (p.eps >= 0.f && bound < 0x1p126f);
+        fp8_path = !qc.fd.fast ? FP8_IEEE : pair_ok ? FP8_PAIR : FP8_CLAMP;
+    }
+    __syncthreads();  // barriers initialised, table filled, warp_ss free again
 
     int s = 0;            // stage of row i (i mod S)
     uint32_t parity = 0;  // phase parity of that stage's barrier ((i / S) mod 2)
@@ -400,7 +434,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
 
         // ---- a = sum of partials (fp32, index order), h = dtype(a + r) ----
         float h[VPT][E];
-        float ss = 0.f;
+        uint64_t ss2 = 0;  // two fp32 partial sums (+0, +0)
 #pragma unroll
         for (int v = 0; v < VPT; ++v)
 #pragma unroll
@@ -426,14 +460,24 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                     Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * p.k + off)
                                          : make_uint4(0, 0, 0, 0), r);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) r[e] = __fadd_rn(hc[e], r[e]);
+                    for (int e = 0; e < 8; e += 2)
+                        upk2(add2(pk2(hc[e], hc[e + 1]), pk2(r[e], r[e + 1])), r[e], r[e + 1]);
                     const uint4 hb = pack8<T>(r);
                     if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, hb);
                     Act<T>::unpack(hb, hc);
                 }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(hc[e], hc[e], ss);
+                for (int e = 0; e < 8; e += 2) {
+                    const uint64_t h2 = pk2(hc[e], hc[e + 1]);
+                    ss2 = fma2(h2, h2, ss2);
+                }
             }
+        float ss;
+        {
+            float a, b;
+            upk2(ss2, a, b);
+            ss = a + b;
+        }
 
         ss = warp_sum(ss);
         if ((t & 31) == 0) warp_ss[i & 1][t >> 5] = ss;
@@ -444,17 +488,21 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         }
         const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
 
-        auto finish = [&](auto fast) {
+        auto finish = [&](auto path) {
+            const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 float yf[E];
 #pragma unroll
-                for (int e = 0; e < E; ++e) yf[e] = __fmul_rn(__fmul_rn(h[v][e], inv), bw[v][e]);
-                epilogue_unit<T, MODE, decltype(fast)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+                for (int e = 0; e < E; e += 2)
+                    upk2(mul2(mul2(pk2(h[v][e], h[v][e + 1]), inv2), pk2(bw[v][e], bw[v][e + 1])),
+                         yf[e], yf[e + 1]);
+                epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, m, row, col[v], ok[v], t);
             }
         };
-        if (MODE != MODE_FP8 || qc.fd.fast) finish(std::true_type{});
-        else finish(std::false_type{});
+        if (MODE != MODE_FP8 || fp8_path == FP8_PAIR) finish(std::integral_constant<int, FP8_PAIR>{});
+        else if (fp8_path == FP8_CLAMP) finish(std::integral_constant<int, FP8_CLAMP>{});
+        else finish(std::integral_constant<int, FP8_IEEE>{});
         if (++s == S) {
             s = 0;
             parity ^= 1u;

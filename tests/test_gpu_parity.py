@@ -272,6 +272,20 @@ def test_streaming_kernel(gnq, dtype, mode, scale, M, H, k, res):
     assert gnq.read_device_error() == 0
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_fp8_clamped_path_with_huge_weights(gnq, kernel):
+    """bf16 weights near 1e36 make y * (1/s) overflow fp32: the kernels must
+    take the clamped quotient and still saturate exactly like the oracle."""
+    M, H = 400, 2048
+    x, r, w = _make(M, H, "bf16", seed=41)
+    w = w.float()
+    w[::5] = 1e36
+    w[1::5] = -3e35
+    w = w.to(torch.bfloat16)
+    with forced_policy(gnq, kernel):
+        run_case(gnq, x, r, w, "fp8", 0.001, write_y=True, dtype="bf16")
+
+
 def test_automatic_policy_large_batch(gnq):
     """The automatic choice for a prefill-sized batch (streaming kernel)."""
     x, r, w = _make(2048, 5120, "bf16", seed=77)
