@@ -192,8 +192,8 @@ int gnq_read_device_error(unsigned int *flags, int clear);
  * Diagnostic: the static-FP8 quantizer the kernels use, applied to n fp32
  * values y (device pointer): q[i] = e4m3_satfinite(y[i] / *scale), with
  * `scale` a device pointer to one fp32.  Values go through it in groups of
- * eight on the path a kernel would take for them (paired arithmetic when
- * every y / s of the group is safely finite, else the clamped or IEEE form).
+ * eight on the path the kernels take (paired arithmetic after the magnitude
+ * clamp applied to bf16 y, or IEEE division for extreme scales).
  * Lets a test sweep every 16-bit y value against an independent encoder.
  */
 int gnq_quantize_fp8_values(const float *y, int64_t n, const float *scale, uint8_t *q,

@@ -112,33 +112,31 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops, in
 }
 
 // Automatic launch shape, from sweeps of every kernel / cluster / chunks-per-
-// thread combination on the decode, prefill and partial-sum workloads:
-//   * M < 16 x SMs (decode batches, mid-size prefill): one CTA per row,
-//     one unit per thread; the row is split over a cluster only when there
-//     are very few rows and they are wide (M x C < 32, >= 2048 elements per
-//     CTA), where the extra SMs outweigh the cluster barrier.
-//   * larger M: rows stream through persistent CTAs of ~256 threads, except
-//     FP8 / MXFP8 / no-quant with a residual and no partials, where a CTA per
-//     row with four units per thread keeps the most loads in flight.
+// thread combination over decode (M = 1..1024), prefill and partial-sum
+// workloads on GB300:
+//   * large batches (M >= 16 x SMs) stream rows through persistent CTAs:
+//     1024 threads for a single FP8 / MXFP8 / no-quant activation with a
+//     residual, ~256 threads otherwise;
+//   * rows of 1024+ units from M >= 3 x SMs also stream (512-thread CTAs);
+//   * otherwise one CTA per row, one unit per thread.  A row is split over a
+//     cluster only when it has more than 1024 units: on these shapes the
+//     cluster barrier always cost more than the extra SMs gave back.
 LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int k, bool res) {
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
     const int nops = k + (res ? 1 : 0);
     LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0};
     const int64_t units = H / unit_elems(mode);
-    int vpt_stream = 1;
-    while (vpt_stream < 4 && (units + vpt_stream - 1) / vpt_stream > 256) vpt_stream *= 2;
     const bool big = M >= 16LL * d.sms;
-    const bool row_big = big && k == 1 && res && mode != MODE_NVFP4;
-    const bool want_stream = fk == 2 || (fk == 0 && big && !row_big);
+    const int64_t target = !big ? 512 : (k == 1 && res && mode != MODE_NVFP4) ? 1024 : 256;
+    int vpt_stream = 1;
+    while (vpt_stream < 4 && (units + vpt_stream - 1) / vpt_stream > target) vpt_stream *= 2;
+    const bool wide = units >= 1024 && M >= 3LL * d.sms;
+    const bool want_stream = fk == 2 || (fk == 0 && (big || wide));
     if (want_stream && stream_shape(d, M, H, mode, nops, fv ? fv : vpt_stream, ls)) return ls;
     if (want_stream && fv && stream_shape(d, M, H, mode, nops, vpt_stream, ls)) return ls;
 
-    if (fk == 0 && row_big) ls.vpt = 4;
     const int64_t gran2 = 2LL * granule(mode);
-    while (ls.cluster < 8 && M * ls.cluster < 32 && H % (gran2 * ls.cluster) == 0 &&
-           H / (2 * ls.cluster) >= 2048)
-        ls.cluster *= 2;
-    // wide rows: a CTA handles at most 1024 units
+    // rows wider than 1024 units: a CTA handles at most 1024 units
     while (ls.cluster < 8 && units / ls.cluster > 1024 && H % (gran2 * ls.cluster) == 0)
         ls.cluster *= 2;
     const int64_t nunits = H / ls.cluster / unit_elems(mode);
@@ -224,35 +222,30 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     return e == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
 }
 
-// Groups of 8 values through the kernels' FP8 encoder, on the path a kernel
-// would take: pairs when every y * (1/s) of the group is finite, else the
-// clamped form (IEEE division for extreme scales); a ragged tail goes
-// through the single-value form.
+// Groups of 8 values through the kernels' FP8 encoder: the paired path
+// with the magnitude clamp the kernels apply to bf16 y (a no-op for
+// bf16/fp16 values that cannot overflow), or IEEE division for extreme
+// scales.  The ragged tail is padded to a group.
 __global__ void fp8_values_kernel(const float *y, int64_t n, const float *scale, uint8_t *q) {
     const Fp8Div fd = make_fp8_div(*scale);
-    const int64_t groups = n / 8;
+    const int64_t groups = (n + 7) / 8;
     for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < groups;
          g += (int64_t)gridDim.x * blockDim.x) {
         float v[8];
-        bool pair_ok = true;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            v[i] = y[8 * g + i];
-            pair_ok = pair_ok && fabsf(v[i]) * fabsf(fd.r) < 0x1p126f;
+            const int64_t j = 8 * g + i;
+            v[i] = j < n ? y[j] : 0.f;
+            if (fd.fast) v[i] = copysignf(min_nan(fabsf(v[i]), fd.ylim), v[i]);
         }
         uint32_t lo, hi;
-        if (!fd.fast) fp8_codes8<FP8_IEEE>(v, fd, lo, hi);
-        else if (pair_ok) fp8_codes8<FP8_PAIR>(v, fd, lo, hi);
-        else fp8_codes8<FP8_CLAMP>(v, fd, lo, hi);
+        if (fd.fast) fp8_codes8<FP8_PAIR>(v, fd, lo, hi);
+        else fp8_codes8<FP8_IEEE>(v, fd, lo, hi);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            q[8 * g + i] = (uint8_t)(lo >> (8 * i));
-            q[8 * g + 4 + i] = (uint8_t)(hi >> (8 * i));
+        for (int i = 0; i < 8; ++i) {
+            const int64_t j = 8 * g + i;
+            if (j < n) q[j] = (uint8_t)((i < 4 ? lo : hi) >> (8 * (i & 3)));
         }
-    }
-    if (blockIdx.x == 0 && threadIdx.x < (n & 7)) {
-        const int64_t i = groups * 8 + threadIdx.x;
-        q[i] = (uint8_t)(e4m3x2(fp8_quotient(y[i], fd), 0.f) & 0xFF);
     }
 }
 
@@ -358,7 +351,7 @@ int gnq_quantize_fp8_values(const float *y, int64_t n, const float *scale, uint8
     if (n < 0) return GNQ_ERR_SHAPE;
     if (n == 0) return GNQ_OK;
     if (!y || !scale || !q) return GNQ_ERR_NULL;
-    const int64_t groups = n / 8 + 1;
+    const int64_t groups = (n + 7) / 8;
     const int64_t blocks = (groups + 255) / 256 < 4096 ? (groups + 255) / 256 : 4096;
     gnq::fp8_values_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         y, n, scale, q);

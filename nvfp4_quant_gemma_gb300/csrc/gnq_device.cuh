@@ -246,24 +246,25 @@ template <int N> __device__ __forceinline__ void mul_arr_s(float *v, float c) {
     for (int i = 0; i < N; i += 2) upk2(mul2(pk2(v[i], v[i + 1]), cc), v[i], v[i + 1]);
 }
 
-// The static FP8 quotient y / s as the E4M3 encoder needs it.  Three paths,
+// The static FP8 quotient y / s as the E4M3 encoder needs it.  Two paths,
 // chosen once per CTA:
-//   FP8_PAIR  (2^-80 <= s <= 2^80 and y * (1/s) provably finite): the
-//             correction step on pairs, in negated form:
-//             n0 = RN(y * -r), rem = y + n0 * s (exact), n1 = RN(rem * -r + n0)
-//             = -RN(y / s) for every y, signed zeros included; the caller
-//             flips the sign bits of the codes.
-//   FP8_CLAMP (2^-80 <= s <= 2^80): |y| first clamped to ylim = 1024 s (a
-//             clamped quotient is >= 1024 and saturates to 448 like the true
-//             one; NaN passes through), the correction step on |y|, the sign
-//             of y put back.
+//   FP8_PAIR  (2^-80 <= s <= 2^80): the correction step on pairs, in negated
+//             form: n0 = RN(y * -r), rem = y + n0 * s (exact),
+//             n1 = RN(rem * -r + n0) = -RN(y / s), signed zeros included; the
+//             code signs are flipped back.  The correction is exact for
+//             |y| >= 2^-103 (below that |y/s| < 2^-23, a zero code of the
+//             right sign either way).  y * (1/s) must be finite: fp16 y is at
+//             most 65504 < 2^126 * s; bf16 y is first clamped to
+//             |y| <= ylim = RD_bf16(1024 s) with its sign kept (any clamped
+//             value has a quotient >= 464 that saturates to 448, like the
+//             true one; NaN passes through).
 //   FP8_IEEE  other scales: IEEE division.
-// The correction is exact for |y| >= 2^-103; below that |y/s| < 2^-23, a
-// zero code of the right sign either way.
-enum { FP8_IEEE = 0, FP8_CLAMP = 1, FP8_PAIR = 2 };
+enum { FP8_IEEE = 0, FP8_PAIR = 2 };
 
 struct Fp8Div {
-    float s, r, ylim;
+    float s, r;
+    uint32_t ylim2;  // RD_bf16(1024 s), in both halves of a bf16x2 word
+    float ylim;      // the same value as fp32
     bool fast;
 };
 
@@ -271,8 +272,10 @@ __device__ __forceinline__ Fp8Div make_fp8_div(float s) {
     Fp8Div d;
     d.s = s;
     d.r = __frcp_rn(s);
-    d.ylim = s * 1024.f;  // exact: power-of-two scaling in range
     d.fast = s >= 0x1p-80f && s <= 0x1p80f;
+    const uint32_t t = __float_as_uint(s * 1024.f) >> 16;  // exact product, then toward zero
+    d.ylim2 = t | (t << 16);
+    d.ylim = __uint_as_float(t << 16);
     return d;
 }
 
@@ -282,7 +285,14 @@ __device__ __forceinline__ float min_nan(float a, float b) {
     return d;
 }
 
-// Eight E4M3 codes of y[0..8) / s (FP8_PAIR: of -(y / s), see above) as two words.
+// Both bf16 halves of v with their magnitude clamped to ylim2's, signs kept.
+__device__ __forceinline__ uint32_t clamp_bf16x2(uint32_t v, uint32_t ylim2) {
+    uint32_t d;
+    asm("min.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(ylim2));
+    return d;
+}
+
+// Eight E4M3 codes of y[0..8) / s as two words (y already clamped for bf16).
 template <int PATH>
 __device__ __forceinline__ void fp8_codes8(const float *y, const Fp8Div &d, uint32_t &lo,
                                            uint32_t &hi) {
@@ -301,25 +311,9 @@ __device__ __forceinline__ void fp8_codes8(const float *y, const Fp8Div &d, uint
         return;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if (PATH == FP8_IEEE) {
-            q[i] = __fdiv_rn(y[i], d.s);
-        } else {
-            const float a = min_nan(fabsf(y[i]), d.ylim);
-            float q0;
-            q[i] = copysignf(div_fma(a, d.s, d.r, q0), y[i]);
-        }
-    }
+    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(y[i], d.s);
     lo = e4m3x4(q[0], q[1], q[2], q[3]);
     hi = e4m3x4(q[4], q[5], q[6], q[7]);
-}
-
-// Single value, for the diagnostic entry point (FP8_CLAMP or FP8_IEEE).
-__device__ __forceinline__ float fp8_quotient(float y, const Fp8Div &d) {
-    if (!d.fast) return __fdiv_rn(y, d.s);
-    const float a = min_nan(fabsf(y), d.ylim);
-    float q0;
-    return copysignf(div_fma(a, d.s, d.r, q0), y);
 }
 
 // amax / 6 correctly rounded (amax >= 0).

@@ -85,8 +85,15 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
     constexpr int U = Unit<MODE>::U;
 #pragma unroll
     for (int c = 0; c < U; ++c) {
-        const uint4 yb = pack8<T>(&yf[8 * c]);
+        uint4 yb = pack8<T>(&yf[8 * c]);
         if (p.write_y && ok) st_v4(p.y + row + col + 8 * c, yb);
+        if (MODE == MODE_FP8 && FP8PATH == FP8_PAIR && std::is_same<T, __nv_bfloat16>::value) {
+            // keep y * (1/s) finite; clamped values still saturate to 448
+            yb.x = clamp_bf16x2(yb.x, qc.fd.ylim2);
+            yb.y = clamp_bf16x2(yb.y, qc.fd.ylim2);
+            yb.z = clamp_bf16x2(yb.z, qc.fd.ylim2);
+            yb.w = clamp_bf16x2(yb.w, qc.fd.ylim2);
+        }
         Act<T>::unpack(yb, &yf[8 * c]);  // the rounded y feeds the quantizer
     }
 
@@ -306,11 +313,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
             epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, m, row, col[v], ok[v], t);
         }
     };
-    // FP8 quotient path: pairs when y * (1/s) cannot overflow (fp16 y is
-    // at most 65504 and |1/s| <= 2^80), else the clamped form.
     if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
-    else if (MODE == MODE_FP8 && !std::is_same<T, __half>::value)
-        finish(std::integral_constant<int, FP8_CLAMP>{});
     else finish(std::integral_constant<int, FP8_PAIR>{});
 
     if (C > 1) cluster_wait();  // peers may still be reading this CTA's partial
@@ -381,29 +384,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
     }
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
-    // FP8 quotient path for this CTA.  Pairs need y * (1/s) finite: fp16 y is
-    // at most 65504; for bf16, |y_j| <= sqrt(H) |bias + w_j| (1 + 2^-8) since
-    // |h_j| / rms(h) <= sqrt(H) when eps >= 0, so a bound on max |bias + w|
-    // decides it.
-    int fp8_path = FP8_PAIR;
-    if (MODE == MODE_FP8) {
-        float wmax = 0.f;
-#pragma unroll
-        for (int v = 0; v < VPT; ++v)
-#pragma unroll
-            for (int i = 0; i < E; ++i) wmax = fmaxf(wmax, fabsf(bw[v][i]));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) wmax = fmaxf(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
-        if ((t & 31) == 0) warp_ss[1][t >> 5] = wmax;
-        __syncthreads();
-        float all = (t & 31) < (NT >> 5) ? warp_ss[1][t & 31] : 0.f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) all = fmaxf(all, __shfl_xor_sync(0xffffffffu, all, o));
-        const float bound = sqrtf((float)p.H) * all * 1.01f * fabsf(qc.fd.r);
-        const bool pair_ok = std::is_same<T, __half>::value || (p.eps >= 0.f && bound < 0x1p126f);
-        fp8_path = !qc.fd.fast ? FP8_IEEE : pair_ok ? FP8_PAIR : FP8_CLAMP;
-    }
-    __syncthreads();  // barriers initialised, table filled, warp_ss free again
+    __syncthreads();  // barriers initialised, table filled
 
     int s = 0;            // stage of row i (i mod S)
     uint32_t parity = 0;  // phase parity of that stage's barrier ((i / S) mod 2)
@@ -500,9 +481,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                 epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, m, row, col[v], ok[v], t);
             }
         };
-        if (MODE != MODE_FP8 || fp8_path == FP8_PAIR) finish(std::integral_constant<int, FP8_PAIR>{});
-        else if (fp8_path == FP8_CLAMP) finish(std::integral_constant<int, FP8_CLAMP>{});
-        else finish(std::integral_constant<int, FP8_IEEE>{});
+        if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
+        else finish(std::integral_constant<int, FP8_PAIR>{});
         if (++s == S) {
             s = 0;
             parity ^= 1u;
