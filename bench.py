@@ -150,6 +150,17 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None}
 
 
+def max_over_ranks(value: float, world: int, dev=None) -> float:
+    """The largest value over all ranks (the slowest replica's time)."""
+    t = torch.tensor([value], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+        if dist.get_backend() == "nccl":
+            t = t.to(dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def device_uuid(dev: torch.device):
     try:
         u = str(torch.cuda.get_device_properties(dev).uuid)
@@ -380,12 +391,7 @@ def run_gnq(args, rank: int, world: int, barrier):
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None
     ms = time_graph(g_timed, dev, args.steps, barrier=barrier, soak_s=args.soak, sampler=sampler)
-    ms_t = torch.tensor([ms], dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-        ms_t = ms_t.to(dev) if dist.get_backend() == "nccl" else ms_t
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, world, dev)
     bytes_step = wl.algorithmic_bytes()
     value = bytes_step * args.steps * world / (ms_max / 1e3) / 1e9
     per_launch_s = ms / 1e3 / args.steps
@@ -396,12 +402,7 @@ def run_gnq(args, rank: int, world: int, barrier):
         # end to end through the public API with host buffers
         e2e_steps = max(1, min(args.steps, 500, int(4e9 // bytes_step)))
         e2e_ms, h2d, d2h = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier)
-        e2e_t = torch.tensor([e2e_ms], dtype=torch.float64)
-        if world > 1:
-            import torch.distributed as dist
-            e2e_t = e2e_t.to(dev) if dist.get_backend() == "nccl" else e2e_t
-            dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-        e2e_value = bytes_step * e2e_steps * world / (float(e2e_t.item()) / 1e3) / 1e9
+        e2e_value = bytes_step * e2e_steps * world / (max_over_ranks(e2e_ms, world, dev) / 1e3) / 1e9
         e2e = {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                "how": "pinned host inputs copied in, op via the Python API, results copied out"}
