@@ -284,7 +284,9 @@ class _Null:
 def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None):
     """Same metric through the public API with host buffers: every step copies
     its inputs from pinned host memory, runs the op, and reads its results
-    back into pinned host memory."""
+    back into pinned host memory.  Steps alternate between two streams with
+    their own device buffers, so one step's copy back overlaps the next
+    step's copy in (separate copy engines) and compute."""
     inp = make_inputs(wl)
     n_host = 4
     host_in = []
@@ -292,45 +294,56 @@ def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None):
         x = inp["x"].clone().pin_memory()
         r = None if inp["residual"] is None else inp["residual"].clone().pin_memory()
         host_in.append((x, r))
-    xd = torch.empty_like(inp["x"], device=dev)
-    rd = None if inp["residual"] is None else torch.empty_like(inp["residual"], device=dev)
     w = inp["weight"].to(dev)
     s = inp["scale"].to(dev)
-    out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, wl.write_y, xd)
-    host_out = [None if t is None else torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                for t in out]
-    host_r = None if rd is None else torch.empty(rd.shape, dtype=rd.dtype, pin_memory=True)
+    lanes = []
+    for _ in range(2):
+        xd = torch.empty_like(inp["x"], device=dev)
+        rd = None if inp["residual"] is None else torch.empty_like(inp["residual"], device=dev)
+        out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, wl.write_y, xd)
+        host_out = [None if t is None else torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for t in out]
+        host_r = None if rd is None else torch.empty(rd.shape, dtype=rd.dtype, pin_memory=True)
+        lanes.append((torch.cuda.Stream(dev), xd, rd, out, host_out, host_r))
     h2d = sum(t.numel() * t.element_size() for t in host_in[0] if t is not None)
-    d2h = sum(t.numel() * t.element_size() for t in host_out if t is not None)
-    d2h += 0 if host_r is None else host_r.numel() * host_r.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in lanes[0][4] if t is not None)
+    d2h += 0 if lanes[0][5] is None else lanes[0][5].numel() * lanes[0][5].element_size()
 
     def one(i):
+        st, xd, rd, out, host_out, host_r = lanes[i % 2]
         hx, hr = host_in[i % n_host]
-        xd.copy_(hx, non_blocking=True)
-        if rd is not None:
-            rd.copy_(hr, non_blocking=True)
-        if wl.k > 1:
-            gnq.gemma_add_rms_norm_quant_parts(xd, rd, w, wl.eps, s, wl.mode, write_y=wl.write_y, out=out)
-        else:
-            gnq.gemma_add_rms_norm_quant(xd, rd, w, wl.eps, s, wl.mode, write_y=wl.write_y, out=out)
-        for h, d in zip(host_out, out):
-            if h is not None:
-                h.copy_(d, non_blocking=True)
-        if rd is not None:
-            host_r.copy_(rd, non_blocking=True)
+        with torch.cuda.stream(st):
+            xd.copy_(hx, non_blocking=True)
+            if rd is not None:
+                rd.copy_(hr, non_blocking=True)
+            if wl.k > 1:
+                gnq.gemma_add_rms_norm_quant_parts(xd, rd, w, wl.eps, s, wl.mode,
+                                                   write_y=wl.write_y, out=out)
+            else:
+                gnq.gemma_add_rms_norm_quant(xd, rd, w, wl.eps, s, wl.mode,
+                                             write_y=wl.write_y, out=out)
+            for h, d in zip(host_out, out):
+                if h is not None:
+                    h.copy_(d, non_blocking=True)
+            if rd is not None:
+                host_r.copy_(rd, non_blocking=True)
 
     for i in range(warmup):
         one(i)
     torch.cuda.synchronize(dev)
     if barrier:
         barrier()
-    stream = torch.cuda.current_stream(dev)
+    main = torch.cuda.current_stream(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
+    e0.record(main)
+    for lane in lanes:
+        lane[0].wait_event(e0)
     for i in range(steps):
         one(i)
-    e1.record(stream)
+    for lane in lanes:
+        main.wait_stream(lane[0])
+    e1.record(main)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1)
     return ms, h2d, d2h

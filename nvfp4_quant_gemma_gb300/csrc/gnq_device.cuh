@@ -125,6 +125,25 @@ template <> struct Act<__half> {
     }
 };
 
+// Correctly rounded 16-bit sums of two packed pairs (equal to the fp32 sum
+// rounded once: the fp32 sum of two 16-bit values cannot land on a 16-bit
+// rounding tie it would not have exactly).
+template <typename T> __device__ __forceinline__ uint32_t add16x2(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t add16x2<__nv_bfloat16>(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+template <> __device__ __forceinline__ uint32_t add16x2<__half>(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+template <typename T> __device__ __forceinline__ uint4 add16x8(uint4 a, uint4 b) {
+    return make_uint4(add16x2<T>(a.x, b.x), add16x2<T>(a.y, b.y), add16x2<T>(a.z, b.z),
+                      add16x2<T>(a.w, b.w));
+}
+
 template <typename T> __device__ __forceinline__ uint4 pack8(const float f[8]) {
     uint4 r;
     r.x = Act<T>::pack2(f[0], f[1]);

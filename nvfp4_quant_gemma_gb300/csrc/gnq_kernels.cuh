@@ -133,11 +133,18 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
     }
 }
 
-// Sum of the per-warp partials in warp_ss[0..nw): each warp reduces them
-// with the same shuffle tree, so every thread gets the same value.
-__device__ __forceinline__ float block_total(const float *warp_ss, int nw, int lane) {
-    float v = lane < nw ? warp_ss[lane] : 0.f;
-    return warp_sum(v);
+// Sum of the per-warp partials in warp_ss[0..32) (entries >= the warp count
+// are zero): every thread reads them with vector loads and adds them in the
+// same fixed tree order, so every thread gets the same value.
+__device__ __forceinline__ float block_total(const float *warp_ss) {
+    const float4 *v = reinterpret_cast<const float4 *>(warp_ss);
+    float4 a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = v[i];
+    float s[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = (a[i].x + a[i].y) + (a[i].z + a[i].w);
+    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
 }
 
 // inv = 1 / sqrt(mean(h^2) + eps); mean via the host-rounded 1/H.
@@ -151,7 +158,7 @@ __device__ __forceinline__ float inv_rms(const Params &p, float tot) {
 template <typename T, int MODE, bool PARTS, int VPT>
 __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
-    __shared__ float warp_ss[32];
+    __shared__ __align__(16) float warp_ss[32];
     __shared__ float cta_ss;
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
@@ -241,15 +248,11 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 #pragma unroll
         for (int c = 0; c < U; ++c) {
             float *hc = &h[v][8 * c];
-            Act<T>::unpack(xv[v][c], hc);
             if (p.residual) {
-                float r[8];
-                Act<T>::unpack(rv[v][c], r);
-#pragma unroll
-                for (int i = 0; i < 8; i += 2)
-                    upk2(add2(pk2(hc[i], hc[i + 1]), pk2(r[i], r[i + 1])), r[i], r[i + 1]);
-                rv[v][c] = pack8<T>(r);  // the new residual, stored below
+                rv[v][c] = add16x8<T>(xv[v][c], rv[v][c]);  // the new residual, stored below
                 Act<T>::unpack(rv[v][c], hc);
+            } else {
+                Act<T>::unpack(xv[v][c], hc);
             }
 #pragma unroll
             for (int i = 0; i < 8; i += 2) {
@@ -280,8 +283,9 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     // ---- row reduction: warps, then CTA, then cluster ----
     ss = warp_sum(ss);
     if ((t & 31) == 0) warp_ss[t >> 5] = ss;
+    if (t < 32 && t >= (NT >> 5)) warp_ss[t] = 0.f;
     __syncthreads();
-    float tot = block_total(warp_ss, NT >> 5, t & 31);
+    float tot = block_total(warp_ss);
     if (C > 1) {
         if (t == 0) cta_ss = tot;
         cluster_arrive_release();
@@ -328,7 +332,7 @@ template <typename T, int MODE, bool PARTS, int VPT>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     extern __shared__ __align__(128) uint8_t dsmem[];
-    __shared__ float warp_ss[2][32];
+    __shared__ __align__(16) float warp_ss[2][32];
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
     const int NT = blockDim.x;
@@ -435,17 +439,14 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                     xv = pack8<T>(acc);
                 }
                 float *hc = &h[v][8 * c];
-                Act<T>::unpack(xv, hc);
                 if (p.residual) {
-                    float r[8];
-                    Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * p.k + off)
-                                         : make_uint4(0, 0, 0, 0), r);
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2)
-                        upk2(add2(pk2(hc[e], hc[e + 1]), pk2(r[e], r[e + 1])), r[e], r[e + 1]);
-                    const uint4 hb = pack8<T>(r);
+                    const uint4 rb = ok[v] ? lds_v4(stage + row_bytes * p.k + off)
+                                           : make_uint4(0, 0, 0, 0);
+                    const uint4 hb = add16x8<T>(xv, rb);
                     if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, hb);
                     Act<T>::unpack(hb, hc);
+                } else {
+                    Act<T>::unpack(xv, hc);
                 }
 #pragma unroll
                 for (int e = 0; e < 8; e += 2) {
@@ -462,12 +463,13 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
 
         ss = warp_sum(ss);
         if ((t & 31) == 0) warp_ss[i & 1][t >> 5] = ss;
+        if (t < 32 && t >= (NT >> 5)) warp_ss[i & 1][t] = 0.f;
         __syncthreads();  // also: every thread is done reading this stage
         if (t == 0 && i + S < n_rows) {
             fence_async_shared();
             issue(i + S, s);
         }
-        const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
+        const float inv = inv_rms(p, block_total(warp_ss[i & 1]));
 
         auto finish = [&](auto path) {
             const uint64_t inv2 = pk2(inv, inv);

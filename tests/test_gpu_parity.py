@@ -331,6 +331,28 @@ def test_special_rows(gnq):
         run_case(gnq, x, r, w, mode, s, write_y=True, dtype="bf16")
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_subnormal_and_cancelling_residuals(gnq, dtype, kernel):
+    """Residual sums that are subnormal, cancel to +-0, or round at ties are
+    bit-exact (the packed 16-bit add keeps subnormals)."""
+    M, H = 300, 1024
+    T = DTYPES[dtype]
+    tiny = 2.0 ** (-133 if dtype == "bf16" else -24)   # smallest subnormal
+    g = torch.Generator().manual_seed(3)
+    x = (torch.randint(-40, 40, (M, H), generator=g).float() * tiny)
+    r = (torch.randint(-40, 40, (M, H), generator=g).float() * tiny)
+    r[::3] = -x[::3]                                    # exact cancellation
+    x[1, :64] = -0.0
+    r[1, :64] = -0.0                                    # -0 + -0 = -0
+    x[5:, :] = torch.randn(M - 5, H, generator=g)       # normal rows for the quantizers
+    x, r = x.to(T), r.to(T)
+    w = torch.randn(H, generator=g).to(T)
+    with forced_policy(gnq, kernel):
+        for mode, s in (("fp8", 0.05), ("nvfp4", 168.0)):
+            run_case(gnq, x, r, w, mode, s, write_y=True, dtype=dtype, check_e2e=False)
+
+
 def test_empty_batch(gnq):
     dev = torch.device("cuda")
     x = torch.empty(0, 128, dtype=torch.bfloat16, device=dev)
