@@ -133,18 +133,12 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
     }
 }
 
-// Sum of the per-warp partials in warp_ss[0..32) (entries >= the warp count
-// are zero): every thread reads them with vector loads and adds them in the
-// same fixed tree order, so every thread gets the same value.
-__device__ __forceinline__ float block_total(const float *warp_ss) {
-    const float4 *v = reinterpret_cast<const float4 *>(warp_ss);
-    float4 a[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) a[i] = v[i];
-    float s[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) s[i] = (a[i].x + a[i].y) + (a[i].z + a[i].w);
-    return ((s[0] + s[1]) + (s[2] + s[3])) + ((s[4] + s[5]) + (s[6] + s[7]));
+// Sum of the per-warp partials in warp_ss[0..nw): each warp reduces them
+// with the same shuffle tree, so every thread gets the same value (one
+// shared load and ten shuffle/add steps per thread, whatever the CTA size).
+__device__ __forceinline__ float block_total(const float *warp_ss, int nw, int lane) {
+    float v = lane < nw ? warp_ss[lane] : 0.f;
+    return warp_sum(v);
 }
 
 // inv = 1 / sqrt(mean(h^2) + eps); mean via the host-rounded 1/H.
@@ -283,9 +277,8 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     // ---- row reduction: warps, then CTA, then cluster ----
     ss = warp_sum(ss);
     if ((t & 31) == 0) warp_ss[t >> 5] = ss;
-    if (t < 32 && t >= (NT >> 5)) warp_ss[t] = 0.f;
     __syncthreads();
-    float tot = block_total(warp_ss);
+    float tot = block_total(warp_ss, NT >> 5, t & 31);
     if (C > 1) {
         if (t == 0) cta_ss = tot;
         cluster_arrive_release();
@@ -463,13 +456,12 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
 
         ss = warp_sum(ss);
         if ((t & 31) == 0) warp_ss[i & 1][t >> 5] = ss;
-        if (t < 32 && t >= (NT >> 5)) warp_ss[i & 1][t] = 0.f;
         __syncthreads();  // also: every thread is done reading this stage
         if (t == 0 && i + S < n_rows) {
             fence_async_shared();
             issue(i + S, s);
         }
-        const float inv = inv_rms(p, block_total(warp_ss[i & 1]));
+        const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
 
         auto finish = [&](auto path) {
             const uint64_t inv2 = pk2(inv, inv);
