@@ -94,6 +94,10 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
 template <typename T> struct Act;
 
 template <> struct Act<__nv_bfloat16> {
+    static __device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
+        lo = __uint_as_float(w << 16);
+        hi = __uint_as_float(w & 0xFFFF0000u);
+    }
     static __device__ __forceinline__ void unpack(uint4 v, float f[8]) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -109,6 +113,11 @@ template <> struct Act<__nv_bfloat16> {
 };
 
 template <> struct Act<__half> {
+    static __device__ __forceinline__ void unpack2(uint32_t w, float &lo, float &hi) {
+        const float2 p = __half22float2(*reinterpret_cast<const __half2 *>(&w));
+        lo = p.x;
+        hi = p.y;
+    }
     static __device__ __forceinline__ void unpack(uint4 v, float f[8]) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -142,6 +151,50 @@ template <> __device__ __forceinline__ uint32_t add16x2<__half>(uint32_t a, uint
 template <typename T> __device__ __forceinline__ uint4 add16x8(uint4 a, uint4 b) {
     return make_uint4(add16x2<T>(a.x, b.x), add16x2<T>(a.y, b.y), add16x2<T>(a.z, b.z),
                       add16x2<T>(a.w, b.w));
+}
+
+// acc + sum of squares of the 8 packed 16-bit values in v: mixed-precision
+// fused multiply-adds (the square of a 16-bit value is exact in fp32, one
+// rounding per add), two chains for latency.
+template <typename T> __device__ __forceinline__ float sumsq16x8(uint4 v, float acc);
+#define GNQ_SUMSQ(TY, PTXT)                                                               \
+    template <> __device__ __forceinline__ float sumsq16x8<TY>(uint4 v, float acc) {     \
+        float a = acc, b = 0.f;                                                           \
+        asm("{\n\t.reg .b16 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"                         \
+            "mov.b32 {l0, h0}, %2;\n\tmov.b32 {l1, h1}, %3;\n\t"                          \
+            "mov.b32 {l2, h2}, %4;\n\tmov.b32 {l3, h3}, %5;\n\t"                          \
+            "fma.rn.f32." PTXT " %0, l0, l0, %0;\n\tfma.rn.f32." PTXT " %1, h0, h0, %1;\n\t" \
+            "fma.rn.f32." PTXT " %0, l1, l1, %0;\n\tfma.rn.f32." PTXT " %1, h1, h1, %1;\n\t" \
+            "fma.rn.f32." PTXT " %0, l2, l2, %0;\n\tfma.rn.f32." PTXT " %1, h2, h2, %1;\n\t" \
+            "fma.rn.f32." PTXT " %0, l3, l3, %0;\n\tfma.rn.f32." PTXT " %1, h3, h3, %1;\n\t}" \
+            : "+f"(a), "+f"(b)                                                            \
+            : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));                                    \
+        return a + b;                                                                     \
+    }
+GNQ_SUMSQ(__nv_bfloat16, "bf16")
+GNQ_SUMSQ(__half, "f16")
+#undef GNQ_SUMSQ
+
+// Per-lane max(|a|, |b|) of two packed pairs (signs of the result are junk).
+template <typename T> __device__ __forceinline__ uint32_t absmax16x2(uint32_t a, uint32_t b);
+template <> __device__ __forceinline__ uint32_t absmax16x2<__nv_bfloat16>(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+template <> __device__ __forceinline__ uint32_t absmax16x2<__half>(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// max |v| over the 16 values of two packed chunks, as fp32 (exact).
+template <typename T> __device__ __forceinline__ float absmax16(uint4 a, uint4 b) {
+    const uint32_t m = absmax16x2<T>(
+        absmax16x2<T>(absmax16x2<T>(a.x, a.y), absmax16x2<T>(a.z, a.w)),
+        absmax16x2<T>(absmax16x2<T>(b.x, b.y), absmax16x2<T>(b.z, b.w)));
+    float lo, hi;
+    Act<T>::unpack2(m, lo, hi);
+    return fmaxf(fabsf(lo), fabsf(hi));
 }
 
 template <typename T> __device__ __forceinline__ uint4 pack8(const float f[8]) {

@@ -75,48 +75,77 @@ __device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, fl
     return qc;
 }
 
+// Output pointers of one row (computed once per row).
+struct RowOut {
+    uint16_t *y;   // y row
+    uint8_t *q;    // code row (FP8/MXFP8: H bytes; NVFP4: H/2 bytes)
+    uint8_t *sf;   // NVFP4: row part of the swizzled scale offsets; MXFP8: scale row
+};
+
+template <int MODE>
+__device__ __forceinline__ RowOut row_out(const Params &p, int64_t m) {
+    RowOut o;
+    const int64_t row = m * (int64_t)p.H;
+    o.y = p.y ? p.y + row : nullptr;
+    o.q = MODE == MODE_NVFP4 ? p.q + (row >> 1) : p.q + row;
+    o.sf = nullptr;
+    if (MODE == MODE_NVFP4)  // tile row, then (m%32)*16 + ((m%128)/32)*4 inside the tile
+        o.sf = p.block_scale + (m >> 7) * (int64_t)p.Kp4 * 512 + (m & 31) * 16 + ((m >> 5) & 3) * 4;
+    if (MODE == MODE_MXFP8) o.sf = p.block_scale + m * (int64_t)(p.H >> 5);
+    return o;
+}
+
+// Column part of the swizzled scale offset of the block starting at `col`.
+__device__ __forceinline__ int sf_col_offset(int col) {
+    const int b = col >> 4;
+    return (b >> 2) * 512 + (b & 3);
+}
+
 // One unit of y (8U values before rounding): round, store y, quantize the
 // rounded values and store codes and scales.  `t` is the thread index;
-// FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA.
+// FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA; `sfc` is the
+// unit's sf_col_offset (NVFP4).
 template <typename T, int MODE, int FP8PATH>
 __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &qc,
-                                              float (&yf)[Unit<MODE>::E], int64_t m, int64_t row,
-                                              int col, bool ok, int t) {
+                                              float (&yf)[Unit<MODE>::E], const RowOut &o,
+                                              int col, int sfc, bool ok, int t) {
     constexpr int U = Unit<MODE>::U;
+    uint4 yb[U];
 #pragma unroll
     for (int c = 0; c < U; ++c) {
-        uint4 yb = pack8<T>(&yf[8 * c]);
-        if (p.write_y && ok) st_v4(p.y + row + col + 8 * c, yb);
-        if (MODE == MODE_FP8 && FP8PATH == FP8_PAIR && std::is_same<T, __nv_bfloat16>::value) {
-            // keep y * (1/s) finite; clamped values still saturate to 448
-            yb.x = clamp_bf16x2(yb.x, qc.fd.ylim2);
-            yb.y = clamp_bf16x2(yb.y, qc.fd.ylim2);
-            yb.z = clamp_bf16x2(yb.z, qc.fd.ylim2);
-            yb.w = clamp_bf16x2(yb.w, qc.fd.ylim2);
-        }
-        Act<T>::unpack(yb, &yf[8 * c]);  // the rounded y feeds the quantizer
+        yb[c] = pack8<T>(&yf[8 * c]);
+        if (p.write_y && ok) st_v4(o.y + col + 8 * c, yb[c]);
     }
 
     if (MODE == MODE_FP8) {
+        uint4 yq = yb[0];
+        if (FP8PATH == FP8_PAIR && std::is_same<T, __nv_bfloat16>::value) {
+            // keep y * (1/s) finite; clamped values still saturate to 448
+            yq.x = clamp_bf16x2(yq.x, qc.fd.ylim2);
+            yq.y = clamp_bf16x2(yq.y, qc.fd.ylim2);
+            yq.z = clamp_bf16x2(yq.z, qc.fd.ylim2);
+            yq.w = clamp_bf16x2(yq.w, qc.fd.ylim2);
+        }
+        Act<T>::unpack(yq, yf);  // the rounded y feeds the quantizer
         uint32_t lo, hi;
         fp8_codes8<FP8PATH>(yf, qc.fd, lo, hi);
-        if (ok) st_v2(p.q + row + col, lo, hi);
+        if (ok) st_v2(o.q + col, lo, hi);
     } else if (MODE == MODE_NVFP4) {
         // one whole 16-element block per unit
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(yf[i]));
+        const float amax = absmax16<T>(yb[0], yb[1]);
         const float sf32 = __fmul_rn(qc.g, div6(amax));
         const uint32_t sf = e4m3x2(sf32, 0.f) & 0xFF;
+        Act<T>::unpack(yb[0], &yf[0]);
+        Act<T>::unpack(yb[1], &yf[8]);
         mul_arr_s<16>(yf, qc.es_tab[sf]);
         const uint32_t lo = e2m1x8(&yf[0]);
         const uint32_t hi = e2m1x8(&yf[8]);
         if (ok) {
-            st_v2(p.q + ((row + col) >> 1), lo, hi);
-            const int b = col >> 4;
-            st_u8(p.block_scale + swizzled_group(m, b & ~3, p.Kp4) + (b & 3), sf);
+            st_v2(o.q + (col >> 1), lo, hi);
+            st_u8(o.sf + sfc, sf);
         }
     } else if (MODE == MODE_MXFP8) {
+        Act<T>::unpack(yb[0], yf);
         float amax = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yf[i]));
@@ -127,9 +156,8 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         mul_arr_s<8>(yf, ldexpf(1.0f, 127 - code));  // y / 2^(code-127), exact
         const uint32_t lo = e4m3x4(yf[0], yf[1], yf[2], yf[3]);
         const uint32_t hi = e4m3x4(yf[4], yf[5], yf[6], yf[7]);
-        if (ok) st_v2(p.q + row + col, lo, hi);
-        if (ok && (t & 3) == 0)
-            st_u8(p.block_scale + m * (int64_t)(p.H >> 5) + (col >> 5), (uint32_t)code);
+        if (ok) st_v2(o.q + col, lo, hi);
+        if (ok && (t & 3) == 0) st_u8(o.sf + (col >> 5), (uint32_t)code);
     }
 }
 
@@ -234,32 +262,16 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
-    // ---- h = dtype(a + residual), sum of squares ----
-    float h[VPT][E];
-    uint64_t ss2 = 0;  // two fp32 partial sums (+0, +0)
+    // ---- h = dtype(a + residual) (kept packed), sum of squares ----
+    uint4 hb[VPT][U];
+    float ss = 0.f;
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int c = 0; c < U; ++c) {
-            float *hc = &h[v][8 * c];
-            if (p.residual) {
-                rv[v][c] = add16x8<T>(xv[v][c], rv[v][c]);  // the new residual, stored below
-                Act<T>::unpack(rv[v][c], hc);
-            } else {
-                Act<T>::unpack(xv[v][c], hc);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const uint64_t h2 = pk2(hc[i], hc[i + 1]);
-                ss2 = fma2(h2, h2, ss2);
-            }
+            hb[v][c] = p.residual ? add16x8<T>(xv[v][c], rv[v][c]) : xv[v][c];
+            ss = sumsq16x8<T>(hb[v][c], ss);
         }
-    float ss;
-    {
-        float a, b;
-        upk2(ss2, a, b);
-        ss = a + b;
-    }
     // A CTA outside a cluster stores the residual now; in a cluster it waits
     // until after the cluster barrier, whose release would otherwise have to
     // wait for these stores.
@@ -269,7 +281,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
             for (int v = 0; v < VPT; ++v)
 #pragma unroll
                 for (int c = 0; c < U; ++c)
-                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, rv[v][c]);
+                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, hb[v][c]);
         }
     };
     if (C == 1) store_residual();
@@ -291,6 +303,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     const float inv = inv_rms(p, tot);
 
     // ---- y = dtype(h * inv * (bias + w)), then quantize the rounded y ----
+    const RowOut o = row_out<MODE>(p, m);
     auto finish = [&](auto path) {
         const uint64_t inv2 = pk2(inv, inv), bias2 = pk2(p.weight_bias, p.weight_bias);
 #pragma unroll
@@ -298,16 +311,18 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
             float yf[E];
 #pragma unroll
             for (int c = 0; c < U; ++c) {
-                float wf[8];
+                float wf[8], hf[8];
                 Act<T>::unpack(wv[v][c], wf);
+                Act<T>::unpack(hb[v][c], hf);
 #pragma unroll
                 for (int i = 0; i < 8; i += 2) {
                     const uint64_t bw2 = add2(bias2, pk2(wf[i], wf[i + 1]));
-                    const uint64_t hi2 = mul2(pk2(h[v][8 * c + i], h[v][8 * c + i + 1]), inv2);
+                    const uint64_t hi2 = mul2(pk2(hf[i], hf[i + 1]), inv2);
                     upk2(mul2(hi2, bw2), yf[8 * c + i], yf[8 * c + i + 1]);
                 }
             }
-            epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+            epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v],
+                                                          sf_col_offset(col[v]), ok[v], t);
         }
     };
     if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
@@ -365,12 +380,14 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
     int col[VPT];
     bool ok[VPT];
     float bw[VPT][E];
+    int sfc[VPT];
     const int nunits = p.H / E;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int u = v * NT + t;
         ok[v] = u < nunits;
         col[v] = u * E;
+        sfc[v] = sf_col_offset(col[v]);
 #pragma unroll
         for (int c = 0; c < U; ++c) {
             const uint4 wv = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
@@ -411,8 +428,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         }
 
         // ---- a = sum of partials (fp32, index order), h = dtype(a + r) ----
-        float h[VPT][E];
-        uint64_t ss2 = 0;  // two fp32 partial sums (+0, +0)
+        uint4 hb[VPT][U];
+        float ss = 0.f;
 #pragma unroll
         for (int v = 0; v < VPT; ++v)
 #pragma unroll
@@ -427,32 +444,20 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                         Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * op + off)
                                              : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], f[e]);
+                        for (int e = 0; e < 8; e += 2)
+                            upk2(add2(pk2(acc[e], acc[e + 1]), pk2(f[e], f[e + 1])), acc[e], acc[e + 1]);
                     }
                     xv = pack8<T>(acc);
                 }
-                float *hc = &h[v][8 * c];
                 if (p.residual) {
                     const uint4 rb = ok[v] ? lds_v4(stage + row_bytes * p.k + off)
                                            : make_uint4(0, 0, 0, 0);
-                    const uint4 hb = add16x8<T>(xv, rb);
-                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, hb);
-                    Act<T>::unpack(hb, hc);
-                } else {
-                    Act<T>::unpack(xv, hc);
+                    xv = add16x8<T>(xv, rb);
+                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, xv);
                 }
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    const uint64_t h2 = pk2(hc[e], hc[e + 1]);
-                    ss2 = fma2(h2, h2, ss2);
-                }
+                hb[v][c] = xv;
+                ss = sumsq16x8<T>(xv, ss);
             }
-        float ss;
-        {
-            float a, b;
-            upk2(ss2, a, b);
-            ss = a + b;
-        }
 
         ss = warp_sum(ss);
         if ((t & 31) == 0) warp_ss[i & 1][t >> 5] = ss;
@@ -463,16 +468,23 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         }
         const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
 
+        const RowOut o = row_out<MODE>(p, m);
         auto finish = [&](auto path) {
             const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
             for (int v = 0; v < VPT; ++v) {
                 float yf[E];
 #pragma unroll
-                for (int e = 0; e < E; e += 2)
-                    upk2(mul2(mul2(pk2(h[v][e], h[v][e + 1]), inv2), pk2(bw[v][e], bw[v][e + 1])),
-                         yf[e], yf[e + 1]);
-                epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, m, row, col[v], ok[v], t);
+                for (int c = 0; c < U; ++c) {
+                    float hf[8];
+                    Act<T>::unpack(hb[v][c], hf);
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        upk2(mul2(mul2(pk2(hf[e], hf[e + 1]), inv2),
+                                  pk2(bw[v][8 * c + e], bw[v][8 * c + e + 1])),
+                             yf[8 * c + e], yf[8 * c + e + 1]);
+                }
+                epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
             }
         };
         if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
