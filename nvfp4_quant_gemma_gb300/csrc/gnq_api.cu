@@ -111,30 +111,47 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops, in
     return false;
 }
 
-// Automatic launch shape, from sweeps of every kernel / cluster / chunks-per-
-// thread combination over decode (M = 1..1024), prefill and partial-sum
-// workloads on GB300:
-//   * large batches (M >= 16 x SMs) stream rows through persistent CTAs:
-//     1024 threads for a single FP8 / MXFP8 / no-quant activation with a
-//     residual, ~256 threads otherwise;
-//   * rows of 1024+ units from M >= 3 x SMs also stream (512-thread CTAs);
-//   * otherwise one CTA per row, one unit per thread.  A row is split over a
-//     cluster only when it has more than 1024 units: on these shapes the
-//     cluster barrier always cost more than the extra SMs gave back.
+// Automatic launch shape, from a sweep of both kernels x chunks per thread x
+// M = 16 .. 16384 on the decode, prefill, no-residual and partial-sum
+// workload classes (GB300, 152 SMs):
+//   * one activation with a residual: one CTA per row at every M -- one
+//     unit per thread below ~SMs rows, else ~256 threads (FP8, MXFP8, no
+//     quant) or ~128 threads (NVFP4) per CTA;
+//   * no residual: one CTA per row up to 16 x SMs rows, then rows stream
+//     through persistent CTAs of ~256 threads;
+//   * k partials: streaming from 4 x SMs rows (~512 threads at 16 x SMs
+//     rows and up, ~256 below), one CTA per row below.
+// A row is split over a cluster only when it has more than 1024 units: on
+// these shapes the cluster barrier always cost more than the extra SMs
+// gave back.
 LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int k, bool res) {
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
     const int nops = k + (res ? 1 : 0);
     LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0};
     const int64_t units = H / unit_elems(mode);
-    const bool big = M >= 16LL * d.sms;
-    const int64_t target = !big ? 512 : (k == 1 && res && mode != MODE_NVFP4) ? 1024 : 256;
-    int vpt_stream = 1;
-    while (vpt_stream < 4 && (units + vpt_stream - 1) / vpt_stream > target) vpt_stream *= 2;
-    const bool wide = units >= 1024 && M >= 3LL * d.sms;
-    const bool want_stream = fk == 2 || (fk == 0 && (big || wide));
-    if (want_stream && stream_shape(d, M, H, mode, nops, fv ? fv : vpt_stream, ls)) return ls;
-    if (want_stream && fv && stream_shape(d, M, H, mode, nops, vpt_stream, ls)) return ls;
+    auto vpt_for = [&](int64_t target) {
+        int v = 1;
+        while (v < 4 && (units + v - 1) / v > target) v *= 2;
+        return v;
+    };
+    const int64_t sms = d.sms;
+    bool stream = false;
+    int vpt = 1;
+    if (k > 1) {
+        stream = M >= 4 * sms;
+        vpt = stream ? vpt_for(M >= 16 * sms ? 512 : 256) : 1;
+    } else if (res) {
+        vpt = M < sms ? 1 : vpt_for(mode == MODE_NVFP4 ? 128 : 256);
+    } else {
+        stream = M >= 16 * sms;
+        vpt = M < sms ? 1 : vpt_for(256);
+    }
+    if (fk) stream = fk == 2;
+    if (fv) vpt = fv;
+    if (stream && stream_shape(d, M, H, mode, nops, vpt, ls)) return ls;
+    if (stream && stream_shape(d, M, H, mode, nops, vpt_for(256), ls)) return ls;
 
+    ls.vpt = fv ? fv : (stream ? 1 : vpt);
     const int64_t gran2 = 2LL * granule(mode);
     // rows wider than 1024 units: a CTA handles at most 1024 units
     while (ls.cluster < 8 && units / ls.cluster > 1024 && H % (gran2 * ls.cluster) == 0)
