@@ -2,6 +2,7 @@
 // launch-shape policy and dispatch.  The contract of every entry point is in
 // include/gemma_nq.h.
 #include <atomic>
+#include <mutex>
 
 #include "gemma_nq.h"
 #include "gnq_launch.cuh"
@@ -15,6 +16,10 @@ extern template cudaError_t launch_mode<MODE_NVFP4>(const Params &, int, bool,
                                                     const LaunchShape &, cudaStream_t);
 extern template cudaError_t launch_mode<MODE_MXFP8>(const Params &, int, bool,
                                                     const LaunchShape &, cudaStream_t);
+extern template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, int, size_t);
+extern template int stream_blocks_per_sm<MODE_FP8>(int, bool, int, int, size_t);
+extern template int stream_blocks_per_sm<MODE_NVFP4>(int, bool, int, int, size_t);
+extern template int stream_blocks_per_sm<MODE_MXFP8>(int, bool, int, int, size_t);
 
 namespace {
 
@@ -81,34 +86,76 @@ bool row_shape_fits(int64_t H, int mode, int cluster, int vpt) {
     return threads <= max_threads(false, vpt);
 }
 
-// Streaming kernel shape: CTAs per SM and ring depth from the shared memory
-// a row needs (operands x 2H bytes per stage); false if it does not fit.
-bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops, int vpt,
-                  LaunchShape &ls) {
+int stream_occupancy_query(int mode, int dtype, bool parts, int vpt, int threads, size_t smem) {
+    switch (mode) {
+        case MODE_NONE: return stream_blocks_per_sm<MODE_NONE>(dtype, parts, vpt, threads, smem);
+        case MODE_FP8: return stream_blocks_per_sm<MODE_FP8>(dtype, parts, vpt, threads, smem);
+        case MODE_NVFP4: return stream_blocks_per_sm<MODE_NVFP4>(dtype, parts, vpt, threads, smem);
+        default: return stream_blocks_per_sm<MODE_MXFP8>(dtype, parts, vpt, threads, smem);
+    }
+}
+
+// Occupancy answers are cached per (device, instance, threads, smem): the
+// query is a driver call, and the answer never changes for a device.
+int stream_occupancy(int mode, int dtype, bool parts, int vpt, int threads, size_t smem) {
+    struct Entry {
+        int dev, mode, dtype, parts, vpt, threads;
+        size_t smem;
+        int blocks;
+    };
+    static std::mutex mu;
+    static Entry cache[256];
+    static int n_cached = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_cached; ++i) {
+            const Entry &e = cache[i];
+            if (e.dev == dev && e.mode == mode && e.dtype == dtype && e.parts == (int)parts &&
+                e.vpt == vpt && e.threads == threads && e.smem == smem)
+                return e.blocks;
+        }
+    }
+    const int blocks = stream_occupancy_query(mode, dtype, parts, vpt, threads, smem);
+    std::lock_guard<std::mutex> lock(mu);
+    if (n_cached < 256) cache[n_cached++] = Entry{dev, mode, dtype, (int)parts, vpt, threads, smem, blocks};
+    return blocks;
+}
+
+// Streaming kernel shape.  For each ring depth S (rows in flight per CTA,
+// 2..4) the occupancy calculator gives the resident CTAs per SM of this
+// instance; the shape with the most resident threads wins (ties: deeper
+// ring).  The grid is one wave of resident CTAs.  False if nothing fits.
+bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, int k, int nops,
+                  int vpt, LaunchShape &ls) {
     if (vpt != 1 && vpt != 2 && vpt != 4) return false;
     const int64_t threads = (H / unit_elems(mode) + vpt - 1) / vpt;
     if (threads > max_threads(true, vpt)) return false;
+    const int64_t thr = (threads + 31) / 32 * 32;
     const int64_t stage = (int64_t)nops * 2 * H;
     if (stage >= (1 << 20)) return false;  // mbarrier transaction count limit
-    const int64_t reserve = 1024 + 2048;   // per-CTA system reserve + static shared memory
-    for (int ctas = 2; ctas >= 1; --ctas) {
-        int64_t budget = d.smem_per_sm / ctas - reserve;
-        if (budget > d.smem_optin) budget = d.smem_optin;
-        int64_t S = budget / stage;
-        if (S > 4) S = 4;
-        if (S >= 2) {
-            ls.stream = true;
-            ls.cluster = 1;
-            ls.vpt = vpt;
-            ls.threads = (int)((threads + 31) / 32 * 32);
-            ls.stages = (int)S;
-            ls.smem = (size_t)(stage * S + 8 * S);
-            ls.grid = M < (int64_t)d.sms * ctas ? M : (int64_t)d.sms * ctas;
-            ls.pdl = g_pdl.load() != 0;
-            return true;
+    int best_blocks = 0, best_S = 0;
+    for (int S = 4; S >= 2; --S) {
+        const int64_t smem = stage * S + 8 * S;
+        if (smem > d.smem_optin) continue;
+        const int blocks = stream_occupancy(mode, dtype, k > 1, vpt, (int)thr, (size_t)smem);
+        if (blocks > best_blocks) {
+            best_blocks = blocks;
+            best_S = S;
         }
     }
-    return false;
+    if (best_blocks == 0) return false;
+    ls.stream = true;
+    ls.cluster = 1;
+    ls.vpt = vpt;
+    ls.threads = (int)thr;
+    ls.stages = best_S;
+    ls.smem = (size_t)(stage * best_S + 8 * best_S);
+    const int64_t wave = (int64_t)d.sms * best_blocks;
+    ls.grid = M < wave ? M : wave;
+    ls.pdl = g_pdl.load() != 0;
+    return true;
 }
 
 // Automatic launch shape, from a sweep of both kernels x chunks per thread x
@@ -124,7 +171,8 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int nops, in
 // A row is split over a cluster only when it has more than 1024 units: on
 // these shapes the cluster barrier always cost more than the extra SMs
 // gave back.
-LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int k, bool res) {
+LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, int k,
+                         bool res) {
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
     const int nops = k + (res ? 1 : 0);
     LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0};
@@ -148,8 +196,8 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int k
     }
     if (fk) stream = fk == 2;
     if (fv) vpt = fv;
-    if (stream && stream_shape(d, M, H, mode, nops, vpt, ls)) return ls;
-    if (stream && stream_shape(d, M, H, mode, nops, vpt_for(256), ls)) return ls;
+    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, ls)) return ls;
+    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), ls)) return ls;
 
     ls.vpt = fv ? fv : (stream ? 1 : vpt);
     const int64_t gran2 = 2LL * granule(mode);
@@ -219,7 +267,7 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 
     const DevInfo *d = dev_info();
     if (!d) return GNQ_ERR_CUDA;
-    const LaunchShape ls = choose_shape(*d, M, H, mode, k, residual != nullptr);
+    const LaunchShape ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr);
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;

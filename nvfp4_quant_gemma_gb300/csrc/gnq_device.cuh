@@ -175,6 +175,28 @@ GNQ_SUMSQ(__nv_bfloat16, "bf16")
 GNQ_SUMSQ(__half, "f16")
 #undef GNQ_SUMSQ
 
+// a_i = RN(h_i * w_i + c_i) for the 8 packed 16-bit h and w and fp32 c: one
+// mixed-precision fused multiply-add each (h * w is exact in fp32).
+template <typename T> __device__ __forceinline__ void fma16x8(uint4 h, uint4 w, float (&c)[8]);
+#define GNQ_FMA16(TY, PTXT)                                                                   \
+    template <> __device__ __forceinline__ void fma16x8<TY>(uint4 h, uint4 w, float (&c)[8]) { \
+        asm("{\n\t.reg .b16 a0, b0, a1, b1, a2, b2, a3, b3, p0, q0, p1, q1, p2, q2, p3, q3;\n\t" \
+            "mov.b32 {a0, b0}, %8;\n\tmov.b32 {a1, b1}, %9;\n\t"                                \
+            "mov.b32 {a2, b2}, %10;\n\tmov.b32 {a3, b3}, %11;\n\t"                              \
+            "mov.b32 {p0, q0}, %12;\n\tmov.b32 {p1, q1}, %13;\n\t"                              \
+            "mov.b32 {p2, q2}, %14;\n\tmov.b32 {p3, q3}, %15;\n\t"                              \
+            "fma.rn.f32." PTXT " %0, a0, p0, %0;\n\tfma.rn.f32." PTXT " %1, b0, q0, %1;\n\t"   \
+            "fma.rn.f32." PTXT " %2, a1, p1, %2;\n\tfma.rn.f32." PTXT " %3, b1, q1, %3;\n\t"   \
+            "fma.rn.f32." PTXT " %4, a2, p2, %4;\n\tfma.rn.f32." PTXT " %5, b2, q2, %5;\n\t"   \
+            "fma.rn.f32." PTXT " %6, a3, p3, %6;\n\tfma.rn.f32." PTXT " %7, b3, q3, %7;\n\t}"  \
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3]), "+f"(c[4]), "+f"(c[5]),            \
+              "+f"(c[6]), "+f"(c[7])                                                              \
+            : "r"(h.x), "r"(h.y), "r"(h.z), "r"(h.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));    \
+    }
+GNQ_FMA16(__nv_bfloat16, "bf16")
+GNQ_FMA16(__half, "f16")
+#undef GNQ_FMA16
+
 // Per-lane max(|a|, |b|) of two packed pairs (signs of the result are junk).
 template <typename T> __device__ __forceinline__ uint32_t absmax16x2(uint32_t a, uint32_t b);
 template <> __device__ __forceinline__ uint32_t absmax16x2<__nv_bfloat16>(uint32_t a, uint32_t b) {

@@ -303,7 +303,12 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     const float inv = inv_rms(p, tot);
 
     // ---- y = dtype(h * inv * (bias + w)), then quantize the rounded y ----
+    // With bias 1 (Gemma) or 0 (plain) the weighted value is one mixed-
+    // precision FMA on the packed h and w: a = RN(h * w + bias * h), then
+    // y = RN(a * inv).
     const RowOut o = row_out<MODE>(p, m);
+    const bool gemma = p.weight_bias == 1.f;
+    const bool plain = p.weight_bias == 0.f;
     auto finish = [&](auto path) {
         const uint64_t inv2 = pk2(inv, inv), bias2 = pk2(p.weight_bias, p.weight_bias);
 #pragma unroll
@@ -311,14 +316,26 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
             float yf[E];
 #pragma unroll
             for (int c = 0; c < U; ++c) {
-                float wf[8], hf[8];
-                Act<T>::unpack(wv[v][c], wf);
-                Act<T>::unpack(hb[v][c], hf);
+                float *a = &yf[8 * c];
+                if (gemma || plain) {
+                    float hw[8];
+                    if (gemma) Act<T>::unpack(hb[v][c], hw);
+                    else
 #pragma unroll
-                for (int i = 0; i < 8; i += 2) {
-                    const uint64_t bw2 = add2(bias2, pk2(wf[i], wf[i + 1]));
-                    const uint64_t hi2 = mul2(pk2(hf[i], hf[i + 1]), inv2);
-                    upk2(mul2(hi2, bw2), yf[8 * c + i], yf[8 * c + i + 1]);
+                        for (int i = 0; i < 8; ++i) hw[i] = 0.f;
+                    fma16x8<T>(hb[v][c], wv[v][c], hw);
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) upk2(mul2(pk2(hw[i], hw[i + 1]), inv2), a[i], a[i + 1]);
+                } else {
+                    float wf[8], hf[8];
+                    Act<T>::unpack(wv[v][c], wf);
+                    Act<T>::unpack(hb[v][c], hf);
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const uint64_t bw2 = add2(bias2, pk2(wf[i], wf[i + 1]));
+                        const uint64_t hi2 = mul2(pk2(hf[i], hf[i + 1]), inv2);
+                        upk2(mul2(hi2, bw2), a[i], a[i + 1]);
+                    }
                 }
             }
             epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v],
@@ -376,10 +393,10 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
     }
 
-    // per-CTA constants: (bias + w) in fp32, quantizer context
+    // per-CTA constants: the packed weight, quantizer context
     int col[VPT];
     bool ok[VPT];
-    float bw[VPT][E];
+    uint4 wq[VPT][U];
     int sfc[VPT];
     const int nunits = p.H / E;
 #pragma unroll
@@ -389,13 +406,10 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         col[v] = u * E;
         sfc[v] = sf_col_offset(col[v]);
 #pragma unroll
-        for (int c = 0; c < U; ++c) {
-            const uint4 wv = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
-            Act<T>::unpack(wv, &bw[v][8 * c]);
-        }
-#pragma unroll
-        for (int i = 0; i < E; ++i) bw[v][i] = __fadd_rn(p.weight_bias, bw[v][i]);
+        for (int c = 0; c < U; ++c)
+            wq[v][c] = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
     }
+    const bool gemma = p.weight_bias == 1.f;
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
     __syncthreads();  // barriers initialised, table filled
@@ -468,6 +482,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         }
         const float inv = inv_rms(p, block_total(warp_ss[i & 1], NT >> 5, t & 31));
 
+        // y = RN(RN(h * w + bias * h) * inv): one mixed-precision FMA on the
+        // packed h and w (exact product), then the scaling.
         const RowOut o = row_out<MODE>(p, m);
         auto finish = [&](auto path) {
             const uint64_t inv2 = pk2(inv, inv);
@@ -476,13 +492,14 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                 float yf[E];
 #pragma unroll
                 for (int c = 0; c < U; ++c) {
-                    float hf[8];
-                    Act<T>::unpack(hb[v][c], hf);
+                    float *a = &yf[8 * c];
+                    if (gemma) Act<T>::unpack(hb[v][c], a);
+                    else
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2)
-                        upk2(mul2(mul2(pk2(hf[e], hf[e + 1]), inv2),
-                                  pk2(bw[v][8 * c + e], bw[v][8 * c + e + 1])),
-                             yf[8 * c + e], yf[8 * c + e + 1]);
+                        for (int e = 0; e < 8; ++e) a[e] = 0.f;
+                    fma16x8<T>(hb[v][c], wq[v][c], *reinterpret_cast<float(*)[8]>(a));
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) upk2(mul2(pk2(a[e], a[e + 1]), inv2), a[e], a[e + 1]);
                 }
                 epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
             }

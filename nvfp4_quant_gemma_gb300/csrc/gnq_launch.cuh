@@ -24,27 +24,47 @@ template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream);
 
+// Resident CTAs per SM of the streaming kernel instance for this shape (0 on
+// error); opts the instance in to `smem` bytes of dynamic shared memory.
+template <int MODE>
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, int threads, size_t smem);
+
 #define GNQ_PICK(K, T, VPT)                                                   \
     (parts ? (void (*)(const Params))K<T, MODE, true, VPT>                     \
            : (void (*)(const Params))K<T, MODE, false, VPT>)
 
 #define GNQ_PICK_VPT(K, T)                                                    \
-    (ls.vpt == 1 ? GNQ_PICK(K, T, 1) : ls.vpt == 2 ? GNQ_PICK(K, T, 2) : GNQ_PICK(K, T, 4))
+    (vpt == 1 ? GNQ_PICK(K, T, 1) : vpt == 2 ? GNQ_PICK(K, T, 2) : GNQ_PICK(K, T, 4))
+
+template <int MODE>
+void (*pick_kernel(int dtype, bool parts, int vpt, bool stream))(const Params) {
+    if (stream)
+        return dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
+                          : GNQ_PICK_VPT(stream_kernel, __half);
+    return dtype == 0 ? GNQ_PICK_VPT(row_kernel, __nv_bfloat16) : GNQ_PICK_VPT(row_kernel, __half);
+}
+
+template <int MODE>
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, int threads, size_t smem) {
+    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, true);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
+        return 0;
+    return n;
+}
 
 template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream) {
-    void (*fn)(const Params) = nullptr;
+    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.stream);
     if (ls.stream) {
-        fn = dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
-                        : GNQ_PICK_VPT(stream_kernel, __half);
         // opt in to the dynamic shared memory this launch needs (idempotent)
         const cudaError_t e = cudaFuncSetAttribute(
             fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem);
         if (e != cudaSuccess) return e;
-    } else {
-        fn = dtype == 0 ? GNQ_PICK_VPT(row_kernel, __nv_bfloat16)
-                        : GNQ_PICK_VPT(row_kernel, __half);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ls.grid, 1, 1);
