@@ -391,7 +391,8 @@ def run_gnq(args, rank: int, world: int, barrier):
     if libbuild.is_stale():
         libbuild.build()
     gnq.load()
-    gnq.set_launch_policy(*[int(v) for v in args.policy.split(",")])
+    pol = [int(v) for v in args.policy.split(",")]
+    gnq.set_launch_policy(*(pol + [0] * (4 - len(pol))))
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
     peak, peak_kind = measured_peak()
@@ -562,8 +563,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-table", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--policy", default="0,0,0",
-                    help="forced launch shape kernel,cluster,vpt (0 = automatic)")
+    ap.add_argument("--policy", default="0,0,0,0",
+                    help="forced launch shape kernel,cluster,vpt,form (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

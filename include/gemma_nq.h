@@ -159,7 +159,11 @@ const char *gnq_status_string(int status);
  *   kernel   0 = automatic; 1 = one CTA (or cluster) per row; 2 = persistent
  *            streaming kernel (rows staged through shared memory).
  *   cluster  row kernel only: 0 = automatic, else 1, 2, 4 or 8 CTAs per row.
- *   vpt      0 = automatic, else 1, 2 or 4 16-byte chunks per thread.
+ *   vpt      0 = automatic, else 1, 2 or 4 units (8 elements; 16 for
+ *            NVFP4) per thread.
+ *   form     0 = automatic; 1 = h and the weight unpacked to fp32 (fewest
+ *            instructions); 2 = kept packed (fewest registers; Gemma or plain
+ *            weight bias only).
  * A forced shape that does not fit a call (H, mode, shared memory) falls back
  * to the automatic one for that call.  The shape only changes the order in
  * which a row's squares are summed (so y may move by one rounding step); the
@@ -167,7 +171,7 @@ const char *gnq_status_string(int status);
  * synchronised with calls in flight on other host threads.  Returns
  * GNQ_ERR_SHAPE for values outside those sets.
  */
-int gnq_set_launch_policy(int kernel, int cluster, int vpt);
+int gnq_set_launch_policy(int kernel, int cluster, int vpt, int form);
 
 /*
  * Programmatic dependent launch (on by default): each launch may start while

@@ -47,7 +47,7 @@ def load() -> ctypes.CDLL:
             "gemma_add_rms_norm_quant": [P, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "gemma_add_rms_norm_quant_parts": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "add_rms_norm_quant": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
-            "gnq_set_launch_policy": [I, I, I],
+            "gnq_set_launch_policy": [I, I, I, I],
             "gnq_read_device_error": [P, I],
             "gnq_set_pdl": [I],
             "gnq_quantize_fp8_values": [P, i64, P, P, P],
@@ -197,10 +197,11 @@ def add_rms_norm_quant(x_parts, residual, weight, eps, scale, mode, write_y=Fals
                        write_y, out, stream)
 
 
-def set_launch_policy(kernel: int = 0, cluster: int = 0, vpt: int = 0) -> None:
+def set_launch_policy(kernel: int = 0, cluster: int = 0, vpt: int = 0, form: int = 0) -> None:
     """Force the launch shape (0 = automatic): kernel 1 = row kernel, 2 =
-    streaming kernel; cluster = CTAs per row; vpt = chunks per thread."""
-    _check(load().gnq_set_launch_policy(int(kernel), int(cluster), int(vpt)),
+    streaming kernel; cluster = CTAs per row; vpt = units per thread; form
+    1 = fp32 (fewest instructions), 2 = packed (fewest registers)."""
+    _check(load().gnq_set_launch_policy(int(kernel), int(cluster), int(vpt), int(form)),
            "gnq_set_launch_policy")
 
 

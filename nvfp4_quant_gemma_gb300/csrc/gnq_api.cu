@@ -16,10 +16,10 @@ extern template cudaError_t launch_mode<MODE_NVFP4>(const Params &, int, bool,
                                                     const LaunchShape &, cudaStream_t);
 extern template cudaError_t launch_mode<MODE_MXFP8>(const Params &, int, bool,
                                                     const LaunchShape &, cudaStream_t);
-extern template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, int, size_t);
-extern template int stream_blocks_per_sm<MODE_FP8>(int, bool, int, int, size_t);
-extern template int stream_blocks_per_sm<MODE_NVFP4>(int, bool, int, int, size_t);
-extern template int stream_blocks_per_sm<MODE_MXFP8>(int, bool, int, int, size_t);
+extern template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_FP8>(int, bool, int, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_NVFP4>(int, bool, int, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_MXFP8>(int, bool, int, bool, int, size_t);
 
 namespace {
 
@@ -44,6 +44,7 @@ DevInfo g_info[kMaxDevices];
 std::atomic<int> g_force_kernel{0};  // 0 auto, 1 row kernel, 2 streaming kernel
 std::atomic<int> g_force_cluster{0};
 std::atomic<int> g_force_vpt{0};
+std::atomic<int> g_force_form{0};  // 0 auto, 1 fp32 form, 2 packed (lean) form
 std::atomic<int> g_pdl{1};  // 1: launch as programmatic dependents, 0: plain launches
 
 // Device properties and the error word's address, queried once per device
@@ -86,20 +87,23 @@ bool row_shape_fits(int64_t H, int mode, int cluster, int vpt) {
     return threads <= max_threads(false, vpt);
 }
 
-int stream_occupancy_query(int mode, int dtype, bool parts, int vpt, int threads, size_t smem) {
+int stream_occupancy_query(int mode, int dtype, bool parts, int vpt, bool lean, int threads,
+                           size_t smem) {
     switch (mode) {
-        case MODE_NONE: return stream_blocks_per_sm<MODE_NONE>(dtype, parts, vpt, threads, smem);
-        case MODE_FP8: return stream_blocks_per_sm<MODE_FP8>(dtype, parts, vpt, threads, smem);
-        case MODE_NVFP4: return stream_blocks_per_sm<MODE_NVFP4>(dtype, parts, vpt, threads, smem);
-        default: return stream_blocks_per_sm<MODE_MXFP8>(dtype, parts, vpt, threads, smem);
+        case MODE_NONE: return stream_blocks_per_sm<MODE_NONE>(dtype, parts, vpt, lean, threads, smem);
+        case MODE_FP8: return stream_blocks_per_sm<MODE_FP8>(dtype, parts, vpt, lean, threads, smem);
+        case MODE_NVFP4:
+            return stream_blocks_per_sm<MODE_NVFP4>(dtype, parts, vpt, lean, threads, smem);
+        default: return stream_blocks_per_sm<MODE_MXFP8>(dtype, parts, vpt, lean, threads, smem);
     }
 }
 
 // Occupancy answers are cached per (device, instance, threads, smem): the
 // query is a driver call, and the answer never changes for a device.
-int stream_occupancy(int mode, int dtype, bool parts, int vpt, int threads, size_t smem) {
+int stream_occupancy(int mode, int dtype, bool parts, int vpt, bool lean, int threads,
+                     size_t smem) {
     struct Entry {
-        int dev, mode, dtype, parts, vpt, threads;
+        int dev, mode, dtype, parts, vpt, lean, threads;
         size_t smem;
         int blocks;
     };
@@ -113,13 +117,14 @@ int stream_occupancy(int mode, int dtype, bool parts, int vpt, int threads, size
         for (int i = 0; i < n_cached; ++i) {
             const Entry &e = cache[i];
             if (e.dev == dev && e.mode == mode && e.dtype == dtype && e.parts == (int)parts &&
-                e.vpt == vpt && e.threads == threads && e.smem == smem)
+                e.vpt == vpt && e.lean == (int)lean && e.threads == threads && e.smem == smem)
                 return e.blocks;
         }
     }
-    const int blocks = stream_occupancy_query(mode, dtype, parts, vpt, threads, smem);
+    const int blocks = stream_occupancy_query(mode, dtype, parts, vpt, lean, threads, smem);
     std::lock_guard<std::mutex> lock(mu);
-    if (n_cached < 256) cache[n_cached++] = Entry{dev, mode, dtype, (int)parts, vpt, threads, smem, blocks};
+    if (n_cached < 256)
+        cache[n_cached++] = Entry{dev, mode, dtype, (int)parts, vpt, (int)lean, threads, smem, blocks};
     return blocks;
 }
 
@@ -128,7 +133,7 @@ int stream_occupancy(int mode, int dtype, bool parts, int vpt, int threads, size
 // instance; the shape with the most resident threads wins (ties: deeper
 // ring).  The grid is one wave of resident CTAs.  False if nothing fits.
 bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, int k, int nops,
-                  int vpt, LaunchShape &ls) {
+                  int vpt, bool lean, LaunchShape &ls) {
     if (vpt != 1 && vpt != 2 && vpt != 4) return false;
     const int64_t threads = (H / unit_elems(mode) + vpt - 1) / vpt;
     if (threads > max_threads(true, vpt)) return false;
@@ -139,7 +144,7 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     for (int S = 4; S >= 2; --S) {
         const int64_t smem = stage * S + 8 * S;
         if (smem > d.smem_optin) continue;
-        const int blocks = stream_occupancy(mode, dtype, k > 1, vpt, (int)thr, (size_t)smem);
+        const int blocks = stream_occupancy(mode, dtype, k > 1, vpt, lean, (int)thr, (size_t)smem);
         if (blocks > best_blocks) {
             best_blocks = blocks;
             best_S = S;
@@ -155,6 +160,7 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     const int64_t wave = (int64_t)d.sms * best_blocks;
     ls.grid = M < wave ? M : wave;
     ls.pdl = g_pdl.load() != 0;
+    ls.lean = lean;
     return true;
 }
 
@@ -172,10 +178,15 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
 // these shapes the cluster barrier always cost more than the extra SMs
 // gave back.
 LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, int k,
-                         bool res) {
+                         bool res, float weight_bias) {
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
+    const int ff = g_force_form.load();
     const int nops = k + (res ? 1 : 0);
-    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0};
+    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false};
+    // The packed (lean) form is chosen where four units per thread would
+    // otherwise cost occupancy; it needs the Gemma or plain weight bias.
+    const bool lean_ok = weight_bias == 1.f || weight_bias == 0.f;
+    auto lean_for = [&](int v) { return lean_ok && (ff ? ff == 2 : v == 4); };
     const int64_t units = H / unit_elems(mode);
     auto vpt_for = [&](int64_t target) {
         int v = 1;
@@ -196,8 +207,9 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     }
     if (fk) stream = fk == 2;
     if (fv) vpt = fv;
-    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, ls)) return ls;
-    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), ls)) return ls;
+    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls)) return ls;
+    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256)), ls))
+        return ls;
 
     ls.vpt = fv ? fv : (stream ? 1 : vpt);
     const int64_t gran2 = 2LL * granule(mode);
@@ -216,6 +228,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     const int64_t threads = (H / ls.cluster / unit_elems(mode) + ls.vpt - 1) / ls.vpt;
     ls.threads = (int)((threads + 31) / 32 * 32);
     ls.grid = M * ls.cluster;
+    ls.lean = lean_for(ls.vpt);
     return ls;
 }
 
@@ -267,7 +280,7 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 
     const DevInfo *d = dev_info();
     if (!d) return GNQ_ERR_CUDA;
-    const LaunchShape ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr);
+    const LaunchShape ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, weight_bias);
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
@@ -374,13 +387,15 @@ const char *gnq_status_string(int status) {
     }
 }
 
-int gnq_set_launch_policy(int kernel, int cluster, int vpt) {
+int gnq_set_launch_policy(int kernel, int cluster, int vpt, int form) {
     if (kernel < 0 || kernel > 2) return GNQ_ERR_SHAPE;
     if (cluster < 0 || cluster > 8 || (cluster & (cluster - 1))) return GNQ_ERR_SHAPE;
     if (vpt != 0 && vpt != 1 && vpt != 2 && vpt != 4) return GNQ_ERR_SHAPE;
+    if (form < 0 || form > 2) return GNQ_ERR_SHAPE;
     gnq::g_force_kernel.store(kernel);
     gnq::g_force_cluster.store(cluster);
     gnq::g_force_vpt.store(vpt);
+    gnq::g_force_form.store(form);
     return GNQ_OK;
 }
 

@@ -177,7 +177,9 @@ __device__ __forceinline__ float inv_rms(const Params &p, float tot) {
 // ---------------------------------------------------------------------------
 // row_kernel: one CTA (or cluster) per row, inputs straight to registers
 // ---------------------------------------------------------------------------
-template <typename T, int MODE, bool PARTS, int VPT>
+// LEAN: h and w stay packed (mixed-precision FMAs; fewest registers).
+// Otherwise h is unpacked once to fp32 (fewest instructions).
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
 __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     __shared__ __align__(16) float warp_ss[32];
@@ -262,16 +264,33 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
-    // ---- h = dtype(a + residual) (kept packed), sum of squares ----
-    uint4 hb[VPT][U];
+    // ---- h = dtype(a + residual), sum of squares ----
+    uint4 hb[VPT][U];                        // packed h (the new residual)
+    float hf[VPT][LEAN ? 1 : E];             // h in fp32 (not LEAN)
     float ss = 0.f;
+    uint64_t ss2 = 0;                        // two fp32 partial sums (not LEAN)
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int c = 0; c < U; ++c) {
             hb[v][c] = p.residual ? add16x8<T>(xv[v][c], rv[v][c]) : xv[v][c];
-            ss = sumsq16x8<T>(hb[v][c], ss);
+            if constexpr (LEAN) {
+                ss = sumsq16x8<T>(hb[v][c], ss);
+            } else {
+                float *hc = &hf[v][8 * c];
+                Act<T>::unpack(hb[v][c], hc);
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) {
+                    const uint64_t h2 = pk2(hc[i], hc[i + 1]);
+                    ss2 = fma2(h2, h2, ss2);
+                }
+            }
         }
+    if constexpr (!LEAN) {
+        float a, b;
+        upk2(ss2, a, b);
+        ss = a + b;
+    }
     // A CTA outside a cluster stores the residual now; in a cluster it waits
     // until after the cluster barrier, whose release would otherwise have to
     // wait for these stores.
@@ -317,7 +336,16 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 #pragma unroll
             for (int c = 0; c < U; ++c) {
                 float *a = &yf[8 * c];
-                if (gemma || plain) {
+                if constexpr (!LEAN) {
+                    float wf[8];
+                    Act<T>::unpack(wv[v][c], wf);
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const uint64_t bw2 = add2(bias2, pk2(wf[i], wf[i + 1]));
+                        const uint64_t hi2 = mul2(pk2(hf[v][8 * c + i], hf[v][8 * c + i + 1]), inv2);
+                        upk2(mul2(hi2, bw2), a[i], a[i + 1]);
+                    }
+                } else if (gemma || plain) {
                     float hw[8];
                     if (gemma) Act<T>::unpack(hb[v][c], hw);
                     else
@@ -353,7 +381,10 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 // ---------------------------------------------------------------------------
 // Dynamic shared memory: stages x operands x (2H bytes), then one mbarrier
 // per stage.  Operands of a row: partial 0..k-1, then the residual.
-template <typename T, int MODE, bool PARTS, int VPT>
+// LEAN: as for row_kernel, the weight kept packed; y comes from the mixed-
+// precision FMA of the bias 1 (Gemma) or bias 0 (plain) form -- the host
+// launches LEAN only for those two biases.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     extern __shared__ __align__(128) uint8_t dsmem[];
@@ -393,10 +424,12 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
     }
 
-    // per-CTA constants: the packed weight, quantizer context
+    // per-CTA constants: the weight (packed if LEAN, else bias + w in fp32),
+    // quantizer context
     int col[VPT];
     bool ok[VPT];
-    uint4 wq[VPT][U];
+    uint4 wq[VPT][LEAN ? U : 1];
+    float bw[VPT][LEAN ? 1 : E];
     int sfc[VPT];
     const int nunits = p.H / E;
 #pragma unroll
@@ -406,8 +439,16 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         col[v] = u * E;
         sfc[v] = sf_col_offset(col[v]);
 #pragma unroll
-        for (int c = 0; c < U; ++c)
-            wq[v][c] = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < U; ++c) {
+            const uint4 w = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
+            if constexpr (LEAN) {
+                wq[v][c] = w;
+            } else {
+                Act<T>::unpack(w, &bw[v][8 * c]);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) bw[v][8 * c + i] = __fadd_rn(p.weight_bias, bw[v][8 * c + i]);
+            }
+        }
     }
     const bool gemma = p.weight_bias == 1.f;
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
@@ -442,8 +483,10 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         }
 
         // ---- a = sum of partials (fp32, index order), h = dtype(a + r) ----
-        uint4 hb[VPT][U];
+        uint4 hb[VPT][LEAN ? U : 1];   // packed h (LEAN)
+        float hf[VPT][LEAN ? 1 : E];   // h in fp32 (not LEAN)
         float ss = 0.f;
+        uint64_t ss2 = 0;
 #pragma unroll
         for (int v = 0; v < VPT; ++v)
 #pragma unroll
@@ -469,9 +512,24 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                     xv = add16x8<T>(xv, rb);
                     if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, xv);
                 }
-                hb[v][c] = xv;
-                ss = sumsq16x8<T>(xv, ss);
+                if constexpr (LEAN) {
+                    hb[v][c] = xv;
+                    ss = sumsq16x8<T>(xv, ss);
+                } else {
+                    float *hc = &hf[v][8 * c];
+                    Act<T>::unpack(xv, hc);
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const uint64_t h2 = pk2(hc[e], hc[e + 1]);
+                        ss2 = fma2(h2, h2, ss2);
+                    }
+                }
             }
+        if constexpr (!LEAN) {
+            float a, b;
+            upk2(ss2, a, b);
+            ss = a + b;
+        }
 
         ss = warp_sum(ss);
         if ((t & 31) == 0) warp_ss[i & 1][t >> 5] = ss;
@@ -493,13 +551,22 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
 #pragma unroll
                 for (int c = 0; c < U; ++c) {
                     float *a = &yf[8 * c];
-                    if (gemma) Act<T>::unpack(hb[v][c], a);
-                    else
+                    if constexpr (LEAN) {
+                        if (gemma) Act<T>::unpack(hb[v][c], a);
+                        else
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) a[e] = 0.f;
-                    fma16x8<T>(hb[v][c], wq[v][c], *reinterpret_cast<float(*)[8]>(a));
+                            for (int e = 0; e < 8; ++e) a[e] = 0.f;
+                        fma16x8<T>(hb[v][c], wq[v][c], *reinterpret_cast<float(*)[8]>(a));
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2) upk2(mul2(pk2(a[e], a[e + 1]), inv2), a[e], a[e + 1]);
+                        for (int e = 0; e < 8; e += 2)
+                            upk2(mul2(pk2(a[e], a[e + 1]), inv2), a[e], a[e + 1]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2)
+                            upk2(mul2(mul2(pk2(hf[v][8 * c + e], hf[v][8 * c + e + 1]), inv2),
+                                      pk2(bw[v][8 * c + e], bw[v][8 * c + e + 1])),
+                                 a[e], a[e + 1]);
+                    }
                 }
                 epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
             }

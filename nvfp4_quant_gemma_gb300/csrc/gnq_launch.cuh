@@ -18,6 +18,7 @@ struct LaunchShape {
     int stages;      // streaming kernel: rows in flight per CTA
     size_t smem;     // streaming kernel: dynamic shared memory bytes
     bool pdl;        // launch as a programmatic dependent of the preceding grid
+    bool lean;       // packed h / w form (fewest registers) instead of fp32 (fewest instructions)
 };
 
 template <int MODE>
@@ -27,17 +28,18 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
 // Resident CTAs per SM of the streaming kernel instance for this shape (0 on
 // error); opts the instance in to `smem` bytes of dynamic shared memory.
 template <int MODE>
-int stream_blocks_per_sm(int dtype, bool parts, int vpt, int threads, size_t smem);
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, int threads, size_t smem);
 
-#define GNQ_PICK(K, T, VPT)                                                   \
-    (parts ? (void (*)(const Params))K<T, MODE, true, VPT>                     \
-           : (void (*)(const Params))K<T, MODE, false, VPT>)
+#define GNQ_PICK_L(K, T, VPT, L)                                              \
+    (parts ? (void (*)(const Params))K<T, MODE, true, VPT, L>                  \
+           : (void (*)(const Params))K<T, MODE, false, VPT, L>)
+#define GNQ_PICK(K, T, VPT) (lean ? GNQ_PICK_L(K, T, VPT, true) : GNQ_PICK_L(K, T, VPT, false))
 
 #define GNQ_PICK_VPT(K, T)                                                    \
     (vpt == 1 ? GNQ_PICK(K, T, 1) : vpt == 2 ? GNQ_PICK(K, T, 2) : GNQ_PICK(K, T, 4))
 
 template <int MODE>
-void (*pick_kernel(int dtype, bool parts, int vpt, bool stream))(const Params) {
+void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream))(const Params) {
     if (stream)
         return dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
                           : GNQ_PICK_VPT(stream_kernel, __half);
@@ -45,8 +47,8 @@ void (*pick_kernel(int dtype, bool parts, int vpt, bool stream))(const Params) {
 }
 
 template <int MODE>
-int stream_blocks_per_sm(int dtype, bool parts, int vpt, int threads, size_t smem) {
-    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, true);
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, int threads, size_t smem) {
+    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, lean, true);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
@@ -59,7 +61,7 @@ int stream_blocks_per_sm(int dtype, bool parts, int vpt, int threads, size_t sme
 template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream) {
-    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.stream);
+    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.lean, ls.stream);
     if (ls.stream) {
         // opt in to the dynamic shared memory this launch needs (idempotent)
         const cudaError_t e = cudaFuncSetAttribute(
@@ -92,5 +94,6 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
 
 #undef GNQ_PICK_VPT
 #undef GNQ_PICK
+#undef GNQ_PICK_L
 
 }  // namespace gnq

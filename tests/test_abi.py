@@ -84,10 +84,11 @@ def test_parts_validation(lib):
     assert f(*args(9, 256)) == 4    # k > 8
     assert f(*args(4, 255)) == 6    # stride below M*H
     assert f(*args(4, 260)) == 6    # stride not a multiple of 8
-    assert lib.gnq_set_launch_policy(0, 3, 0) == 2
-    assert lib.gnq_set_launch_policy(0, 0, 3) == 2
-    assert lib.gnq_set_launch_policy(3, 0, 0) == 2
-    assert lib.gnq_set_launch_policy(0, 0, 0) == 0
+    assert lib.gnq_set_launch_policy(0, 3, 0, 0) == 2
+    assert lib.gnq_set_launch_policy(0, 0, 3, 0) == 2
+    assert lib.gnq_set_launch_policy(3, 0, 0, 0) == 2
+    assert lib.gnq_set_launch_policy(0, 0, 0, 3) == 2
+    assert lib.gnq_set_launch_policy(0, 0, 0, 0) == 0
     assert lib.gnq_read_device_error(None, 0) == 1
 
 

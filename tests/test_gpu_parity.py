@@ -34,7 +34,7 @@ def gnq():
     build.build()
     import nvfp4_quant_gemma_gb300 as pkg
     pkg.load()
-    pkg.set_launch_policy(0, 0, 0)
+    pkg.set_launch_policy(0, 0, 0, 0)
     oracle.build()
     import os
     oracle.set_threads(os.cpu_count() or 1)
@@ -217,9 +217,11 @@ def test_partials(gnq, k, mode, scale):
 
 
 @pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0)])
-def test_plain_rmsnorm_variant(gnq, mode, scale):
+@pytest.mark.parametrize("kernel,form", [(1, 1), (1, 2), (2, 1), (2, 2)])
+def test_plain_rmsnorm_variant(gnq, mode, scale, kernel, form):
     x, r, w = _make(100, 2048, "bf16", seed=3, w_std=1.0)
-    run_case(gnq, x, r, w, mode, scale, write_y=True, dtype="bf16", weight_bias=0.0)
+    with forced_policy(gnq, kernel, 0, 0, form):
+        run_case(gnq, x, r, w, mode, scale, write_y=True, dtype="bf16", weight_bias=0.0)
 
 
 def test_odd_h_fp8(gnq):
@@ -235,22 +237,24 @@ def test_max_h(gnq):
 
 
 class forced_policy:
-    def __init__(self, gnq, kernel, cluster=0, vpt=0):
-        self.gnq, self.args = gnq, (kernel, cluster, vpt)
+    def __init__(self, gnq, kernel, cluster=0, vpt=0, form=0):
+        self.gnq, self.args = gnq, (kernel, cluster, vpt, form)
 
     def __enter__(self):
         self.gnq.set_launch_policy(*self.args)
 
     def __exit__(self, *exc):
-        self.gnq.set_launch_policy(0, 0, 0)
+        self.gnq.set_launch_policy(0, 0, 0, 0)
 
 
 @pytest.mark.parametrize("kernel,cluster,vpt", [(1, c, v) for c in (1, 2, 4, 8) for v in (1, 2, 4)]
                          + [(2, 0, v) for v in (1, 2, 4)])
-def test_every_launch_shape(gnq, kernel, cluster, vpt):
-    """Forced kernels, cluster sizes and chunks per thread give the same contract."""
+@pytest.mark.parametrize("form", [1, 2])
+def test_every_launch_shape(gnq, kernel, cluster, vpt, form):
+    """Forced kernels, cluster sizes, units per thread and register forms
+    give the same contract."""
     x, r, w = _make(133, 4096, "bf16", seed=cluster * 10 + vpt + kernel)
-    with forced_policy(gnq, kernel, cluster, vpt):
+    with forced_policy(gnq, kernel, cluster, vpt, form):
         run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
         run_case(gnq, x, r, w, "mxfp8", 0.0, write_y=False, dtype="bf16")
         run_case(gnq, x, r, w, "fp8", 0.05, write_y=False, dtype="bf16")
@@ -262,11 +266,13 @@ def test_every_launch_shape(gnq, kernel, cluster, vpt):
 @pytest.mark.parametrize("M,H,k,res", [(1, 64, 1, True), (7, 2048, 1, False), (333, 5120, 1, True),
                                        (1000, 8192, 1, True), (610, 7168, 4, True),
                                        (300, 16384, 1, True), (160, 1024, 3, False)])
-def test_streaming_kernel(gnq, dtype, mode, scale, M, H, k, res):
+@pytest.mark.parametrize("form", [1, 2])
+def test_streaming_kernel(gnq, dtype, mode, scale, M, H, k, res, form):
     """The persistent shared-memory-ring kernel on ragged row counts (rows per
-    CTA differ), every mode, with and without residual and partials."""
+    CTA differ), every mode, with and without residual and partials, in both
+    register forms."""
     x, r, w = _make(M, H, dtype, seed=M + H + k, k=k, residual=res)
-    with forced_policy(gnq, 2):
+    with forced_policy(gnq, 2, 0, 0, form):
         run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 0), dtype=dtype,
                  check_e2e=(M * H >= 1e5))
     assert gnq.read_device_error() == 0
