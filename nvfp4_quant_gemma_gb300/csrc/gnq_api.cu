@@ -164,14 +164,15 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     return true;
 }
 
-// Automatic launch shape, from a sweep of both kernels x chunks per thread x
-// M = 16 .. 16384 on the decode, prefill, no-residual and partial-sum
-// workload classes (GB300, 152 SMs):
+// Automatic launch shape, from sweeps of both kernels x units per thread x
+// register form x M = 16 .. 16384 on the decode, prefill, no-residual and
+// partial-sum workload classes (GB300, 152 SMs):
 //   * one activation with a residual: one CTA per row at every M -- one
 //     unit per thread below ~SMs rows, else ~256 threads (FP8, MXFP8, no
-//     quant) or ~128 threads (NVFP4) per CTA;
+//     quant) or ~160 threads (NVFP4) per CTA;
 //   * no residual: one CTA per row up to 16 x SMs rows, then rows stream
-//     through persistent CTAs of ~256 threads;
+//     through persistent CTAs of four units per thread (~256 threads for
+//     FP8 at H = 8192, ~128 for NVFP4);
 //   * k partials: streaming from 4 x SMs rows (~512 threads at 16 x SMs
 //     rows and up, ~256 below), one CTA per row below.
 // A row is split over a cluster only when it has more than 1024 units: on
@@ -184,9 +185,13 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     const int nops = k + (res ? 1 : 0);
     LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false};
     // The packed (lean) form is chosen where four units per thread would
-    // otherwise cost occupancy; it needs the Gemma or plain weight bias.
+    // otherwise cost occupancy -- except in the streaming FP8 / MXFP8 /
+    // no-quant kernel, which is instruction-bound -- and needs the Gemma or
+    // plain weight bias.
     const bool lean_ok = weight_bias == 1.f || weight_bias == 0.f;
-    auto lean_for = [&](int v) { return lean_ok && (ff ? ff == 2 : v == 4); };
+    auto lean_for = [&](int v, bool stream) {
+        return lean_ok && (ff ? ff == 2 : v == 4 && !(stream && mode != MODE_NVFP4));
+    };
     const int64_t units = H / unit_elems(mode);
     auto vpt_for = [&](int64_t target) {
         int v = 1;
@@ -200,15 +205,17 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
         stream = M >= 4 * sms;
         vpt = stream ? vpt_for(M >= 16 * sms ? 512 : 256) : 1;
     } else if (res) {
-        vpt = M < sms ? 1 : vpt_for(mode == MODE_NVFP4 ? 128 : 256);
+        vpt = M < sms ? 1 : vpt_for(mode == MODE_NVFP4 ? 160 : 256);
     } else {
         stream = M >= 16 * sms;
-        vpt = M < sms ? 1 : vpt_for(256);
+        vpt = M < sms ? 1 : vpt_for(stream && mode == MODE_NVFP4 ? 128 : 256);
     }
     if (fk) stream = fk == 2;
     if (fv) vpt = fv;
-    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls)) return ls;
-    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256)), ls))
+    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt, true), ls))
+        return ls;
+    if (stream &&
+        stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256), true), ls))
         return ls;
 
     ls.vpt = fv ? fv : (stream ? 1 : vpt);
@@ -228,7 +235,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     const int64_t threads = (H / ls.cluster / unit_elems(mode) + ls.vpt - 1) / ls.vpt;
     ls.threads = (int)((threads + 31) / 32 * 32);
     ls.grid = M * ls.cluster;
-    ls.lean = lean_for(ls.vpt);
+    ls.lean = lean_for(ls.vpt, false);
     return ls;
 }
 
