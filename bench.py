@@ -40,9 +40,9 @@ from nvfp4_quant_gemma_gb300.workloads import HEADLINE, WORKLOADS, DTYPES, make_
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s for add+GemmaRMSNorm+quant"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["nvfp4_quant_gemma_gb300/csrc/gnq_kernels.cuh",
-                  "nvfp4_quant_gemma_gb300/csrc/gnq_launch.cuh",
-                  "nvfp4_quant_gemma_gb300/csrc/gnq_api.cu"]
+KERNEL_SOURCES = ["nvfp4_quant_gemma_gb300/csrc/" + f for f in (
+    "gnq_device.cuh", "gnq_kernels.cuh", "gnq_launch.cuh", "gnq_api.cu", "gnq_mode_none.cu",
+    "gnq_mode_fp8.cu", "gnq_mode_nvfp4.cu", "gnq_mode_mxfp8.cu")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
