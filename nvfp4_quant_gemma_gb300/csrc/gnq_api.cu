@@ -140,9 +140,12 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     const int64_t thr = (threads + 31) / 32 * 32;
     const int64_t stage = (int64_t)nops * 2 * H;
     if (stage >= (1 << 20)) return false;  // mbarrier transaction count limit
+    // fp32 bias + w table of the register-light form (see stream_kernel)
+    const int64_t wtab = (!lean && vpt >= 2 && mode == MODE_NVFP4) ? 4 * H : 0;
+    auto smem_for = [&](int S) { return (stage * S + 8 * S + 15) / 16 * 16 + wtab; };
     int best_blocks = 0, best_S = 0;
     for (int S = 4; S >= 2; --S) {
-        const int64_t smem = stage * S + 8 * S;
+        const int64_t smem = smem_for(S);
         if (smem > d.smem_optin) continue;
         const int blocks = stream_occupancy(mode, dtype, k > 1, vpt, lean, (int)thr, (size_t)smem);
         if (blocks > best_blocks) {
@@ -156,7 +159,7 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     ls.vpt = vpt;
     ls.threads = (int)thr;
     ls.stages = best_S;
-    ls.smem = (size_t)(stage * best_S + 8 * best_S);
+    ls.smem = (size_t)smem_for(best_S);
     const int64_t wave = (int64_t)d.sms * best_blocks;
     ls.grid = M < wave ? M : wave;
     ls.pdl = g_pdl.load() != 0;
@@ -173,8 +176,8 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
 //   * no residual: one CTA per row up to 16 x SMs rows, then rows stream
 //     through persistent CTAs of four units per thread (~256 threads for
 //     FP8 at H = 8192, ~128 for NVFP4);
-//   * k partials: streaming from 4 x SMs rows (~512 threads at 16 x SMs
-//     rows and up, ~256 below), one CTA per row below.
+//   * k partials: streaming from 4 x SMs rows (~256 threads; FP8 / MXFP8 /
+//     no quant ~512 from 16 x SMs rows), one CTA per row below.
 // A row is split over a cluster only when it has more than 1024 units: on
 // these shapes the cluster barrier always cost more than the extra SMs
 // gave back.
@@ -203,7 +206,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     int vpt = 1;
     if (k > 1) {
         stream = M >= 4 * sms;
-        vpt = stream ? vpt_for(M >= 16 * sms ? 512 : 256) : 1;
+        vpt = stream ? vpt_for(M >= 16 * sms && mode != MODE_NVFP4 ? 512 : 256) : 1;
     } else if (res) {
         vpt = M < sms ? 1 : vpt_for(mode == MODE_NVFP4 ? 160 : 256);
     } else {

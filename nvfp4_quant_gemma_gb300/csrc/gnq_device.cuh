@@ -79,6 +79,24 @@ __device__ __forceinline__ void st_u32(void *p, uint32_t a) {
 __device__ __forceinline__ void st_u8(void *p, uint32_t a) {
     asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(a) : "memory");
 }
+// Predicated stores: the store is skipped when `on` is false, without a
+// branch, so the code around it stays one basic block.
+__device__ __forceinline__ void st_v4_if(void *p, uint4 v, bool on) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t"
+                 "@q st.global.v4.u32 [%0], {%1,%2,%3,%4};\n\t}" ::"l"(p),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"((int)on)
+                 : "memory");
+}
+__device__ __forceinline__ void st_v2_if(void *p, uint32_t a, uint32_t b, bool on) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t"
+                 "@q st.global.v2.u32 [%0], {%1,%2};\n\t}" ::"l"(p), "r"(a), "r"(b), "r"((int)on)
+                 : "memory");
+}
+__device__ __forceinline__ void st_u8_if(void *p, uint32_t a, bool on) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+                 "@q st.global.u8 [%0], %1;\n\t}" ::"l"(p), "r"(a), "r"((int)on)
+                 : "memory");
+}
 
 __device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
     uint4 r;
@@ -410,12 +428,15 @@ __device__ __forceinline__ void fp8_codes8(const float *y, const Fp8Div &d, uint
     hi = e4m3x4(q[4], q[5], q[6], q[7]);
 }
 
-// amax / 6 correctly rounded (amax >= 0).
+// amax / 6 correctly rounded, for amax the magnitude of a 16-bit value (0,
+// finite, inf or NaN).  The correction step above is exact for every finite
+// bf16 and fp16 magnitude, subnormals and the largest bf16 values included
+// (an exhaustive check in exact rational arithmetic), and gives 0 for 0 and
+// NaN for NaN; only inf needs its own answer.
 __device__ __forceinline__ float div6(float amax) {
-    if (!(amax >= 0x1p-100f) || amax > 0x1p120f) return __fdiv_rn(amax, 6.0f);
     float q0;
     const float q1 = div_fma(amax, 6.0f, 0.16666667163372039794921875f /* RN(1/6) */, q0);
-    return q1;
+    return amax == __int_as_float(0x7F800000) ? amax : q1;
 }
 
 // ---------------------------------------------------------------------------

@@ -101,6 +101,28 @@ __device__ __forceinline__ int sf_col_offset(int col) {
     return (b >> 2) * 512 + (b & 3);
 }
 
+// Out-of-range units (a row that is not a whole number of units per
+// thread).  NVFP4 (Pred<MODE>): such a unit loads an in-range unit instead,
+// adds nothing to the sum of squares and its stores are predicated off, so
+// the long per-unit epilogue stays one basic block.  The other modes branch
+// around the unit's loads (zero-filled) and stores, which measured faster
+// for their shorter epilogues.
+template <int MODE> struct Pred {
+    static constexpr bool value = MODE == MODE_NVFP4;
+};
+template <bool PRED> __device__ __forceinline__ void st_v4_unit(void *p, uint4 v, bool ok) {
+    if constexpr (PRED) st_v4_if(p, v, ok);
+    else if (ok) st_v4(p, v);
+}
+template <bool PRED> __device__ __forceinline__ void st_v2_unit(void *p, uint32_t a, uint32_t b, bool ok) {
+    if constexpr (PRED) st_v2_if(p, a, b, ok);
+    else if (ok) st_v2(p, a, b);
+}
+template <bool PRED> __device__ __forceinline__ void st_u8_unit(void *p, uint32_t a, bool ok) {
+    if constexpr (PRED) st_u8_if(p, a, ok);
+    else if (ok) st_u8(p, a);
+}
+
 // One unit of y (8U values before rounding): round, store y, quantize the
 // rounded values and store codes and scales.  `t` is the thread index;
 // FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA; `sfc` is the
@@ -114,7 +136,8 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
 #pragma unroll
     for (int c = 0; c < U; ++c) {
         yb[c] = pack8<T>(&yf[8 * c]);
-        if (p.write_y && ok) st_v4(o.y + col + 8 * c, yb[c]);
+        if (Pred<MODE>::value ? p.write_y != 0 : p.write_y && ok)
+            st_v4_unit<Pred<MODE>::value>(o.y + col + 8 * c, yb[c], ok);
     }
 
     if (MODE == MODE_FP8) {
@@ -129,7 +152,7 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         Act<T>::unpack(yq, yf);  // the rounded y feeds the quantizer
         uint32_t lo, hi;
         fp8_codes8<FP8PATH>(yf, qc.fd, lo, hi);
-        if (ok) st_v2(o.q + col, lo, hi);
+        st_v2_unit<false>(o.q + col, lo, hi, ok);
     } else if (MODE == MODE_NVFP4) {
         // one whole 16-element block per unit
         const float amax = absmax16<T>(yb[0], yb[1]);
@@ -140,10 +163,8 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         mul_arr_s<16>(yf, qc.es_tab[sf]);
         const uint32_t lo = e2m1x8(&yf[0]);
         const uint32_t hi = e2m1x8(&yf[8]);
-        if (ok) {
-            st_v2(o.q + (col >> 1), lo, hi);
-            st_u8(o.sf + sfc, sf);
-        }
+        st_v2_unit<true>(o.q + (col >> 1), lo, hi, ok);
+        st_u8_unit<true>(o.sf + sfc, sf, ok);
     } else if (MODE == MODE_MXFP8) {
         Act<T>::unpack(yb[0], yf);
         float amax = 0.f;
@@ -156,8 +177,8 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         mul_arr_s<8>(yf, ldexpf(1.0f, 127 - code));  // y / 2^(code-127), exact
         const uint32_t lo = e4m3x4(yf[0], yf[1], yf[2], yf[3]);
         const uint32_t hi = e4m3x4(yf[4], yf[5], yf[6], yf[7]);
-        if (ok) st_v2(o.q + col, lo, hi);
-        if (ok && (t & 3) == 0) st_u8(o.sf + (col >> 5), (uint32_t)code);
+        st_v2_unit<false>(o.q + col, lo, hi, ok);
+        st_u8_unit<false>(o.sf + (col >> 5), (uint32_t)code, ok && (t & 3) == 0);
     }
 }
 
@@ -179,12 +200,25 @@ __device__ __forceinline__ float inv_rms(const Params &p, float tot) {
 // ---------------------------------------------------------------------------
 // LEAN: h and w stay packed (mixed-precision FMAs; fewest registers).
 // Otherwise h is unpacked once to fp32 (fewest instructions).
+// Register budget of an NVFP4 row instance (row_kernel_nvfp4; the other
+// modes leave the choice to the compiler, which an explicit budget, even
+// one equal to the launch bound's, was measured to change for the worse).
+// The forms the launch policy picks for one activation get four resident
+// CTAs at their thread counts (160 threads at four 16-byte chunks per
+// thread, 128 at eight); the others keep what 1024 / VPT threads allow.
+template <int MODE, int VPT, bool PARTS, bool LEAN> struct RowForm {
+    static constexpr int U = Unit<MODE>::U, chunks = VPT * U;
+    static constexpr int cap = VPT == 1 ? 64 : VPT == 2 ? 128 : 255;
+    static constexpr int occ = chunks <= 2 ? 64
+                               : chunks == 4 ? (U == 2 ? 96 : LEAN ? 64 : cap)
+                                             : (LEAN ? 128 : cap);
+    static constexpr int maxnreg = PARTS ? cap : occ;
+};
+
 template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
-__global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
+__device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float &cta_ss,
+                                         float *es_smem) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
-    __shared__ __align__(16) float warp_ss[32];
-    __shared__ float cta_ss;
-    __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
     const uint32_t C = cluster_size();
     const uint32_t rank = C > 1 ? cluster_rank() : 0;
@@ -194,13 +228,15 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     const int nunits = p.seg / E;
     const int64_t row = m * (int64_t)p.H;
 
-    int col[VPT];
+    constexpr bool PRED = Pred<MODE>::value;
+    int col[VPT], lc[VPT];  // lc: the column a unit loads (PRED: clamped in range)
     bool ok[VPT];
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int u = v * NT + t;
         ok[v] = u < nunits;
         col[v] = (int)rank * p.seg + u * E;
+        lc[v] = PRED && !ok[v] ? (int)rank * p.seg : col[v];
     }
 
     pdl_wait();  // inputs may come from the preceding grid
@@ -213,8 +249,8 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
         for (int c = 0; c < U; ++c) {
-            rv[v][c] = (p.residual && ok[v]) ? ld_inout(p.residual + row + col[v] + 8 * c) : zero;
-            xv[v][c] = ok[v] ? ld_stream(p.x + row + col[v] + 8 * c) : zero;
+            rv[v][c] = (p.residual && (PRED || ok[v])) ? ld_inout(p.residual + row + lc[v] + 8 * c) : zero;
+            xv[v][c] = (PRED || ok[v]) ? ld_stream(p.x + row + lc[v] + 8 * c) : zero;
         }
     if (PARTS) {
         // a = dtype(((p0 + p1) + p2) + ...), fp32 accumulation in index order.
@@ -234,7 +270,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
                 for (int v = 0; v < VPT; ++v)
 #pragma unroll
                     for (int c = 0; c < U; ++c)
-                        pv[j][v][c] = (p0 + j < p.k && ok[v]) ? ld_stream(xp + col[v] + 8 * c) : zero;
+                        pv[j][v][c] = (p0 + j < p.k && (PRED || ok[v])) ? ld_stream(xp + lc[v] + 8 * c) : zero;
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -260,33 +296,48 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
-        for (int c = 0; c < U; ++c) wv[v][c] = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : zero;
+        for (int c = 0; c < U; ++c) wv[v][c] = (PRED || ok[v]) ? ld_weight(p.w + lc[v] + 8 * c) : zero;
 
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
     // ---- h = dtype(a + residual), sum of squares ----
     uint4 hb[VPT][U];                        // packed h (the new residual)
     float hf[VPT][LEAN ? 1 : E];             // h in fp32 (not LEAN)
+    // PRED: a sum per unit, masked; otherwise one running sum (zero-filled
+    // out-of-range units add nothing).
     float ss = 0.f;
     uint64_t ss2 = 0;                        // two fp32 partial sums (not LEAN)
 #pragma unroll
-    for (int v = 0; v < VPT; ++v)
+    for (int v = 0; v < VPT; ++v) {
+        float sv = 0.f;
+        uint64_t sv2 = 0;
+        float &acc = PRED ? sv : ss;
+        uint64_t &acc2 = PRED ? sv2 : ss2;
 #pragma unroll
         for (int c = 0; c < U; ++c) {
             hb[v][c] = p.residual ? add16x8<T>(xv[v][c], rv[v][c]) : xv[v][c];
             if constexpr (LEAN) {
-                ss = sumsq16x8<T>(hb[v][c], ss);
+                acc = sumsq16x8<T>(hb[v][c], acc);
             } else {
                 float *hc = &hf[v][8 * c];
                 Act<T>::unpack(hb[v][c], hc);
 #pragma unroll
                 for (int i = 0; i < 8; i += 2) {
                     const uint64_t h2 = pk2(hc[i], hc[i + 1]);
-                    ss2 = fma2(h2, h2, ss2);
+                    acc2 = fma2(h2, h2, acc2);
                 }
             }
         }
-    if constexpr (!LEAN) {
+        if constexpr (PRED) {
+            if constexpr (!LEAN) {
+                float a, b;
+                upk2(sv2, a, b);
+                sv = a + b;
+            }
+            ss += ok[v] ? sv : 0.f;
+        }
+    }
+    if constexpr (!PRED && !LEAN) {
         float a, b;
         upk2(ss2, a, b);
         ss = a + b;
@@ -300,7 +351,7 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
             for (int v = 0; v < VPT; ++v)
 #pragma unroll
                 for (int c = 0; c < U; ++c)
-                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, hb[v][c]);
+                    st_v4_unit<PRED>(p.residual + row + col[v] + 8 * c, hb[v][c], ok[v]);
         }
     };
     if (C == 1) store_residual();
@@ -376,20 +427,54 @@ __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__
     if (C > 1) cluster_wait();  // peers may still be reading this CTA's partial
 }
 
+#define GNQ_ROW_SMEM                                  \
+    __shared__ __align__(16) float warp_ss[32];       \
+    __shared__ float cta_ss;                          \
+    __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
+
+// FP8, MXFP8 and no-quant rows: the compiler's own register choice.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+__global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
+    GNQ_ROW_SMEM
+    row_body<T, MODE, PARTS, VPT, LEAN>(p, warp_ss, cta_ss, es_smem);
+}
+
+// NVFP4 rows: the RowForm register budget.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+__global__ void __launch_bounds__(1024 / VPT) __maxnreg__((RowForm<MODE, VPT, PARTS, LEAN>::maxnreg))
+    row_kernel_nvfp4(const __grid_constant__ Params p) {
+    static_assert(MODE == MODE_NVFP4, "NVFP4 rows only");
+    GNQ_ROW_SMEM
+    row_body<T, MODE, PARTS, VPT, LEAN>(p, warp_ss, cta_ss, es_smem);
+}
+#undef GNQ_ROW_SMEM
+
 // ---------------------------------------------------------------------------
 // stream_kernel: persistent CTAs, rows streamed through a shared-memory ring
 // ---------------------------------------------------------------------------
 // Dynamic shared memory: stages x operands x (2H bytes), then one mbarrier
-// per stage.  Operands of a row: partial 0..k-1, then the residual.
+// per stage, then (StreamForm::smem_w) the fp32 table of bias + w.
+// Operands of a row: partial 0..k-1, then the residual.
 // LEAN: as for row_kernel, the weight kept packed; y comes from the mixed-
 // precision FMA of the bias 1 (Gemma) or bias 0 (plain) form -- the host
 // launches LEAN only for those two biases.
+// NVFP4, not LEAN, several units per thread: bias + w lives in shared
+// memory (chunk j of unit u at float4 index j * H/E + u, so a warp's reads
+// are conflict-free), which frees the registers for a third resident CTA.
+// maxnreg: the register budget of the NVFP4 instances (stream_kernel_nvfp4):
+// 80 for the shared-memory-weight form at two units per thread (three
+// resident CTAs of 256 threads), else what the launch bound allows.
+template <int MODE, int VPT, bool LEAN> struct StreamForm {
+    static constexpr bool smem_w = !LEAN && VPT >= 2 && MODE == MODE_NVFP4;
+    static constexpr int maxnreg = VPT == 1 ? 64 : (smem_w && VPT <= 2 ? 80 : 128);
+};
+
 template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
-__global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
+__device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, float (*warp_ss)[32],
+                                            float *es_smem) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
-    extern __shared__ __align__(128) uint8_t dsmem[];
-    __shared__ __align__(16) float warp_ss[2][32];
-    __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
+    constexpr bool SW = StreamForm<MODE, VPT, LEAN>::smem_w;
+    constexpr bool PRED = Pred<MODE>::value;
 
     const int NT = blockDim.x;
     const int t = threadIdx.x;
@@ -400,6 +485,8 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
     const uint32_t stage_bytes = row_bytes * nops;
     const uint32_t base = (uint32_t)__cvta_generic_to_shared(dsmem);
     const uint32_t bars = base + stage_bytes * S;  // 8-byte aligned: row_bytes % 16 == 0
+    // bias + w table (SW): 16-byte aligned, after the barriers
+    float4 *const bw_s = reinterpret_cast<float4 *>(dsmem + ((stage_bytes * S + 8u * S + 15u) & ~15u));
 
     // rows of this CTA: m_i = blockIdx.x + i * G, i < n_rows
     const int n_rows = p.M > blockIdx.x ? (int)((p.M - 1 - blockIdx.x) / G + 1) : 0;
@@ -429,24 +516,35 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
     int col[VPT];
     bool ok[VPT];
     uint4 wq[VPT][LEAN ? U : 1];
-    float bw[VPT][LEAN ? 1 : E];
+    float bw[VPT][LEAN || SW ? 1 : E];
     int sfc[VPT];
+    int lc[VPT];  // the column a unit loads (PRED: clamped in range)
     const int nunits = p.H / E;
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int u = v * NT + t;
         ok[v] = u < nunits;
         col[v] = u * E;
+        lc[v] = PRED && !ok[v] ? 0 : col[v];
         sfc[v] = sf_col_offset(col[v]);
 #pragma unroll
         for (int c = 0; c < U; ++c) {
-            const uint4 w = ok[v] ? ld_weight(p.w + col[v] + 8 * c) : make_uint4(0, 0, 0, 0);
+            const uint4 w = (PRED || ok[v]) ? ld_weight(p.w + lc[v] + 8 * c) : make_uint4(0, 0, 0, 0);
             if constexpr (LEAN) {
                 wq[v][c] = w;
             } else {
-                Act<T>::unpack(w, &bw[v][8 * c]);
+                float f[8];
+                Act<T>::unpack(w, f);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) bw[v][8 * c + i] = __fadd_rn(p.weight_bias, bw[v][8 * c + i]);
+                for (int i = 0; i < 8; ++i) f[i] = __fadd_rn(p.weight_bias, f[i]);
+                if constexpr (SW) {  // read back only by this thread (SW implies PRED)
+                    const int uu = lc[v] / E;
+                    bw_s[(2 * c) * nunits + uu] = make_float4(f[0], f[1], f[2], f[3]);
+                    bw_s[(2 * c + 1) * nunits + uu] = make_float4(f[4], f[5], f[6], f[7]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) bw[v][8 * c + i] = f[i];
+                }
             }
         }
     }
@@ -485,21 +583,26 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         // ---- a = sum of partials (fp32, index order), h = dtype(a + r) ----
         uint4 hb[VPT][LEAN ? U : 1];   // packed h (LEAN)
         float hf[VPT][LEAN ? 1 : E];   // h in fp32 (not LEAN)
+        const uint4 zero = make_uint4(0, 0, 0, 0);
         float ss = 0.f;
         uint64_t ss2 = 0;
 #pragma unroll
-        for (int v = 0; v < VPT; ++v)
+        for (int v = 0; v < VPT; ++v) {
+            float sv = 0.f;
+            uint64_t sv2 = 0;
+            float &acc_s = PRED ? sv : ss;
+            uint64_t &acc_s2 = PRED ? sv2 : ss2;
+            const bool ld = PRED || ok[v];
 #pragma unroll
             for (int c = 0; c < U; ++c) {
-                const uint32_t off = (uint32_t)(col[v] + 8 * c) * 2u;
-                uint4 xv = ok[v] ? lds_v4(stage + off) : make_uint4(0, 0, 0, 0);
+                const uint32_t off = (uint32_t)(lc[v] + 8 * c) * 2u;
+                uint4 xv = ld ? lds_v4(stage + off) : zero;
                 if (PARTS) {
                     float acc[8];
                     Act<T>::unpack(xv, acc);
                     for (int op = 1; op < p.k; ++op) {
                         float f[8];
-                        Act<T>::unpack(ok[v] ? lds_v4(stage + row_bytes * op + off)
-                                             : make_uint4(0, 0, 0, 0), f);
+                        Act<T>::unpack(ld ? lds_v4(stage + row_bytes * op + off) : zero, f);
 #pragma unroll
                         for (int e = 0; e < 8; e += 2)
                             upk2(add2(pk2(acc[e], acc[e + 1]), pk2(f[e], f[e + 1])), acc[e], acc[e + 1]);
@@ -507,25 +610,32 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                     xv = pack8<T>(acc);
                 }
                 if (p.residual) {
-                    const uint4 rb = ok[v] ? lds_v4(stage + row_bytes * p.k + off)
-                                           : make_uint4(0, 0, 0, 0);
-                    xv = add16x8<T>(xv, rb);
-                    if (ok[v]) st_v4(p.residual + row + col[v] + 8 * c, xv);
+                    xv = add16x8<T>(xv, ld ? lds_v4(stage + row_bytes * p.k + off) : zero);
+                    st_v4_unit<PRED>(p.residual + row + col[v] + 8 * c, xv, ok[v]);
                 }
                 if constexpr (LEAN) {
                     hb[v][c] = xv;
-                    ss = sumsq16x8<T>(xv, ss);
+                    acc_s = sumsq16x8<T>(xv, acc_s);
                 } else {
                     float *hc = &hf[v][8 * c];
                     Act<T>::unpack(xv, hc);
 #pragma unroll
                     for (int e = 0; e < 8; e += 2) {
                         const uint64_t h2 = pk2(hc[e], hc[e + 1]);
-                        ss2 = fma2(h2, h2, ss2);
+                        acc_s2 = fma2(h2, h2, acc_s2);
                     }
                 }
             }
-        if constexpr (!LEAN) {
+            if constexpr (PRED) {
+                if constexpr (!LEAN) {
+                    float a, b;
+                    upk2(sv2, a, b);
+                    sv = a + b;
+                }
+                ss += ok[v] ? sv : 0.f;
+            }
+        }
+        if constexpr (!PRED && !LEAN) {
             float a, b;
             upk2(ss2, a, b);
             ss = a + b;
@@ -561,10 +671,21 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
                         for (int e = 0; e < 8; e += 2)
                             upk2(mul2(pk2(a[e], a[e + 1]), inv2), a[e], a[e + 1]);
                     } else {
+                        float b[8];
+                        if constexpr (SW) {
+                            const int uu = lc[v] / E;
+                            const float4 b0 = bw_s[(2 * c) * nunits + uu];
+                            const float4 b1 = bw_s[(2 * c + 1) * nunits + uu];
+                            b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+                            b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) b[e] = bw[v][8 * c + e];
+                        }
 #pragma unroll
                         for (int e = 0; e < 8; e += 2)
                             upk2(mul2(mul2(pk2(hf[v][8 * c + e], hf[v][8 * c + e + 1]), inv2),
-                                      pk2(bw[v][8 * c + e], bw[v][8 * c + e + 1])),
+                                      pk2(b[e], b[e + 1])),
                                  a[e], a[e + 1]);
                     }
                 }
@@ -579,5 +700,27 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
         }
     }
 }
+
+#define GNQ_STREAM_SMEM                                     \
+    extern __shared__ __align__(128) uint8_t dsmem[];       \
+    __shared__ __align__(16) float warp_ss[2][32];          \
+    __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
+
+// FP8, MXFP8 and no-quant streaming: the compiler's own register choice.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+__global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
+    GNQ_STREAM_SMEM
+    stream_body<T, MODE, PARTS, VPT, LEAN>(p, dsmem, warp_ss, es_smem);
+}
+
+// NVFP4 streaming: the StreamForm register budget.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+__global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) __maxnreg__((StreamForm<MODE, VPT, LEAN>::maxnreg))
+    stream_kernel_nvfp4(const __grid_constant__ Params p) {
+    static_assert(MODE == MODE_NVFP4, "NVFP4 streaming only");
+    GNQ_STREAM_SMEM
+    stream_body<T, MODE, PARTS, VPT, LEAN>(p, dsmem, warp_ss, es_smem);
+}
+#undef GNQ_STREAM_SMEM
 
 }  // namespace gnq

@@ -40,10 +40,18 @@ int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, int threads,
 
 template <int MODE>
 void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream))(const Params) {
-    if (stream)
-        return dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
-                          : GNQ_PICK_VPT(stream_kernel, __half);
-    return dtype == 0 ? GNQ_PICK_VPT(row_kernel, __nv_bfloat16) : GNQ_PICK_VPT(row_kernel, __half);
+    if constexpr (MODE == MODE_NVFP4) {
+        if (stream)
+            return dtype == 0 ? GNQ_PICK_VPT(stream_kernel_nvfp4, __nv_bfloat16)
+                              : GNQ_PICK_VPT(stream_kernel_nvfp4, __half);
+        return dtype == 0 ? GNQ_PICK_VPT(row_kernel_nvfp4, __nv_bfloat16)
+                          : GNQ_PICK_VPT(row_kernel_nvfp4, __half);
+    } else {
+        if (stream)
+            return dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
+                              : GNQ_PICK_VPT(stream_kernel, __half);
+        return dtype == 0 ? GNQ_PICK_VPT(row_kernel, __nv_bfloat16) : GNQ_PICK_VPT(row_kernel, __half);
+    }
 }
 
 template <int MODE>
