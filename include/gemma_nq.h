@@ -177,8 +177,9 @@ int gnq_set_launch_policy(int kernel, int cluster, int vpt, int form);
  * Programmatic dependent launch (on by default): each launch may start while
  * the preceding kernel on the stream drains, and waits inside the kernel
  * (griddepcontrol.wait) until that kernel's results are visible before its
- * first global read; a launch that fits the GPU in one wave also lets the
- * kernel that follows it start early.  Results are identical either way.
+ * first global read; once all of its CTAs have started it also lets a
+ * programmatic dependent that follows it launch (that kernel must wait in the
+ * same way before reading these outputs).  Results are identical either way.
  * enable = 0 turns it off for later calls in this process, 1 turns it on.
  */
 int gnq_set_pdl(int enable);

@@ -294,9 +294,6 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
-    // Dependents may launch at once when this grid is resident in one wave
-    // (it cannot be starved of SMs by them); otherwise at its completion.
-    p.pdl_early = ls.pdl && (ls.stream || ls.grid * ls.threads <= 2048LL * d->sms / 2) ? 1 : 0;
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool parts = k > 1;

@@ -34,7 +34,6 @@ struct Params {
     int seg;              // elements owned by one CTA (H / cluster size)
     int write_y;
     int stages;           // streaming kernel: rows in flight per CTA
-    int pdl_early;        // let dependent grids launch as soon as this one starts
     unsigned int *err;    // device error word
 };
 
@@ -193,27 +192,43 @@ GNQ_SUMSQ(__nv_bfloat16, "bf16")
 GNQ_SUMSQ(__half, "f16")
 #undef GNQ_SUMSQ
 
-// a_i = RN(h_i * w_i + c_i) for the 8 packed 16-bit h and w and fp32 c: one
-// mixed-precision fused multiply-add each (h * w is exact in fp32).
-template <typename T> __device__ __forceinline__ void fma16x8(uint4 h, uint4 w, float (&c)[8]);
-#define GNQ_FMA16(TY, PTXT)                                                                   \
-    template <> __device__ __forceinline__ void fma16x8<TY>(uint4 h, uint4 w, float (&c)[8]) { \
-        asm("{\n\t.reg .b16 a0, b0, a1, b1, a2, b2, a3, b3, p0, q0, p1, q1, p2, q2, p3, q3;\n\t" \
-            "mov.b32 {a0, b0}, %8;\n\tmov.b32 {a1, b1}, %9;\n\t"                                \
-            "mov.b32 {a2, b2}, %10;\n\tmov.b32 {a3, b3}, %11;\n\t"                              \
-            "mov.b32 {p0, q0}, %12;\n\tmov.b32 {p1, q1}, %13;\n\t"                              \
-            "mov.b32 {p2, q2}, %14;\n\tmov.b32 {p3, q3}, %15;\n\t"                              \
-            "fma.rn.f32." PTXT " %0, a0, p0, %0;\n\tfma.rn.f32." PTXT " %1, b0, q0, %1;\n\t"   \
-            "fma.rn.f32." PTXT " %2, a1, p1, %2;\n\tfma.rn.f32." PTXT " %3, b1, q1, %3;\n\t"   \
-            "fma.rn.f32." PTXT " %4, a2, p2, %4;\n\tfma.rn.f32." PTXT " %5, b2, q2, %5;\n\t"   \
-            "fma.rn.f32." PTXT " %6, a3, p3, %6;\n\tfma.rn.f32." PTXT " %7, b3, q3, %7;\n\t}"  \
-            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3]), "+f"(c[4]), "+f"(c[5]),            \
-              "+f"(c[6]), "+f"(c[7])                                                              \
-            : "r"(h.x), "r"(h.y), "r"(h.z), "r"(h.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w));    \
+// a_i = RN(h_i * w_i + h_i * b) for the 8 packed 16-bit h and w and a 16-bit
+// b (the low half of `b16`) that is 0 or 1: h_i * b is formed exactly by a
+// first mixed-precision FMA (addend -0, so it is h_i, +-0 or -0), then the
+// product with w is added in a second (h * w exact, one rounding).  No
+// select on the bias, no fp32 copy of h.
+template <typename T> __device__ __forceinline__ void biasfma16x8(uint4 h, uint4 w, uint32_t b16, float (&c)[8]);
+#define GNQ_BFMA16(TY, PTXT)                                                                     \
+    template <>                                                                                  \
+    __device__ __forceinline__ void biasfma16x8<TY>(uint4 h, uint4 w, uint32_t b16, float (&c)[8]) { \
+        asm("{\n\t.reg .b16 a0, b0, a1, b1, a2, b2, a3, b3, p0, q0, p1, q1, p2, q2, p3, q3, bb, bz;\n\t" \
+            ".reg .f32 t0, t1, t2, t3, t4, t5, t6, t7;\n\t"                                          \
+            "mov.b32 {a0, b0}, %8;\n\tmov.b32 {a1, b1}, %9;\n\t"                                  \
+            "mov.b32 {a2, b2}, %10;\n\tmov.b32 {a3, b3}, %11;\n\t"                                \
+            "mov.b32 {p0, q0}, %12;\n\tmov.b32 {p1, q1}, %13;\n\t"                                \
+            "mov.b32 {p2, q2}, %14;\n\tmov.b32 {p3, q3}, %15;\n\t"                                \
+            "mov.b32 {bb, bz}, %16;\n\t"                                                            \
+            "fma.rn.f32." PTXT " t0, a0, bb, 0f80000000;\n\tfma.rn.f32." PTXT " t1, b0, bb, 0f80000000;\n\t" \
+            "fma.rn.f32." PTXT " t2, a1, bb, 0f80000000;\n\tfma.rn.f32." PTXT " t3, b1, bb, 0f80000000;\n\t" \
+            "fma.rn.f32." PTXT " t4, a2, bb, 0f80000000;\n\tfma.rn.f32." PTXT " t5, b2, bb, 0f80000000;\n\t" \
+            "fma.rn.f32." PTXT " t6, a3, bb, 0f80000000;\n\tfma.rn.f32." PTXT " t7, b3, bb, 0f80000000;\n\t" \
+            "fma.rn.f32." PTXT " %0, a0, p0, t0;\n\tfma.rn.f32." PTXT " %1, b0, q0, t1;\n\t"     \
+            "fma.rn.f32." PTXT " %2, a1, p1, t2;\n\tfma.rn.f32." PTXT " %3, b1, q1, t3;\n\t"     \
+            "fma.rn.f32." PTXT " %4, a2, p2, t4;\n\tfma.rn.f32." PTXT " %5, b2, q2, t5;\n\t"     \
+            "fma.rn.f32." PTXT " %6, a3, p3, t6;\n\tfma.rn.f32." PTXT " %7, b3, q3, t7;\n\t}"    \
+            : "=f"(c[0]), "=f"(c[1]), "=f"(c[2]), "=f"(c[3]), "=f"(c[4]), "=f"(c[5]),             \
+              "=f"(c[6]), "=f"(c[7])                                                                \
+            : "r"(h.x), "r"(h.y), "r"(h.z), "r"(h.w), "r"(w.x), "r"(w.y), "r"(w.z), "r"(w.w),      \
+              "r"(b16));                                                                            \
     }
-GNQ_FMA16(__nv_bfloat16, "bf16")
-GNQ_FMA16(__half, "f16")
-#undef GNQ_FMA16
+GNQ_BFMA16(__nv_bfloat16, "bf16")
+GNQ_BFMA16(__half, "f16")
+#undef GNQ_BFMA16
+
+// 1.0 as a 16-bit pattern of T.
+template <typename T> __device__ __forceinline__ uint32_t one16();
+template <> __device__ __forceinline__ uint32_t one16<__nv_bfloat16>() { return 0x3F80u; }
+template <> __device__ __forceinline__ uint32_t one16<__half>() { return 0x3C00u; }
 
 // Per-lane max(|a|, |b|) of two packed pairs (signs of the result are junk).
 template <typename T> __device__ __forceinline__ uint32_t absmax16x2(uint32_t a, uint32_t b);

@@ -31,8 +31,11 @@
 // (see gnq_device.cuh), so codes are exactly those of the fp32 reading.
 //
 // Both kernels wait on the preceding grid (programmatic dependent launch)
-// before their first global read, so they may be launched while it drains;
-// with `pdl_early` they also let their own dependents launch at once.
+// before their first global read, so they may be launched while it drains,
+// and every CTA then lets the dependent grid launch: it launches once all of
+// this grid's CTAs have started (so it never takes their place), and its
+// CTAs fill the SMs this grid's last wave leaves idle while they wait for
+// this grid's results.
 #pragma once
 
 #include <type_traits>
@@ -240,7 +243,7 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     }
 
     pdl_wait();  // inputs may come from the preceding grid
-    if (p.pdl_early) pdl_trigger();
+    pdl_trigger();
 
     // ---- issue every load of the row segment up front ----
     uint4 rv[VPT][U], xv[VPT][U], wv[VPT][U];
@@ -379,6 +382,7 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     const RowOut o = row_out<MODE>(p, m);
     const bool gemma = p.weight_bias == 1.f;
     const bool plain = p.weight_bias == 0.f;
+    const uint32_t b16 = gemma ? one16<T>() : 0u;  // the bias as a 16-bit value (LEAN)
     auto finish = [&](auto path) {
         const uint64_t inv2 = pk2(inv, inv), bias2 = pk2(p.weight_bias, p.weight_bias);
 #pragma unroll
@@ -398,11 +402,7 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
                     }
                 } else if (gemma || plain) {
                     float hw[8];
-                    if (gemma) Act<T>::unpack(hb[v][c], hw);
-                    else
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) hw[i] = 0.f;
-                    fma16x8<T>(hb[v][c], wv[v][c], hw);
+                    biasfma16x8<T>(hb[v][c], wv[v][c], b16, hw);
 #pragma unroll
                     for (int i = 0; i < 8; i += 2) upk2(mul2(pk2(hw[i], hw[i + 1]), inv2), a[i], a[i + 1]);
                 } else {
@@ -503,7 +503,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
     };
 
     pdl_wait();  // inputs may come from the preceding grid
-    if (p.pdl_early) pdl_trigger();
+    pdl_trigger();
 
     if (t == 0) {
         for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
@@ -548,7 +548,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
             }
         }
     }
-    const bool gemma = p.weight_bias == 1.f;
+    const uint32_t b16 = p.weight_bias == 1.f ? one16<T>() : 0u;  // LEAN: bias 1 or 0
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
     __syncthreads();  // barriers initialised, table filled
@@ -662,11 +662,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                 for (int c = 0; c < U; ++c) {
                     float *a = &yf[8 * c];
                     if constexpr (LEAN) {
-                        if (gemma) Act<T>::unpack(hb[v][c], a);
-                        else
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) a[e] = 0.f;
-                        fma16x8<T>(hb[v][c], wq[v][c], *reinterpret_cast<float(*)[8]>(a));
+                        biasfma16x8<T>(hb[v][c], wq[v][c], b16, *reinterpret_cast<float(*)[8]>(a));
 #pragma unroll
                         for (int e = 0; e < 8; e += 2)
                             upk2(mul2(pk2(a[e], a[e + 1]), inv2), a[e], a[e + 1]);

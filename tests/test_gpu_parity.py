@@ -395,24 +395,32 @@ def test_stream_and_graph_capture(gnq):
         assert torch.equal(yy, y1) and torch.equal(rr, r1)
 
 
-@pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0)])
-def test_pdl_on_and_off_agree(gnq, mode, scale):
+@pytest.mark.parametrize("mode,scale,M,k", [("fp8", 0.05, 256, 1), ("nvfp4", 168.0, 256, 1),
+                                            ("fp8", 0.05, 4096, 1), ("nvfp4", 168.0, 4096, 1),
+                                            ("nvfp4", 168.0, 4096, 2), ("fp8", 0.05, 4096, 2)])
+def test_pdl_on_and_off_agree(gnq, mode, scale, M, k):
     """Programmatic dependent launch changes launch timing only: a chain of
     dependent calls (each consuming the previous residual) gives the same
-    bits with it on and off, eagerly and in a captured graph."""
+    bits with it on and off, eagerly and in a captured graph -- one-wave and
+    many-wave row grids, and the persistent streaming grid (k partials)."""
     dev = torch.device("cuda")
-    x, r, w = _make(256, 4096, "bf16", seed=31)
+    x, r, w = _make(M, 4096, "bf16", seed=31)
     xd, wd = x.to(dev), w.to(dev)
+    if k > 1:
+        xd = torch.stack([xd, (xd * 0.5).to(xd.dtype)])
     sd = torch.tensor([scale], device=dev)
 
     def chain(pdl, graph):
         gnq.set_pdl(pdl)
         try:
             rd = r.to(dev)
-            outs = [gnq.alloc_outputs(256, 4096, mode, True, xd) for _ in range(4)]
+            outs = [gnq.alloc_outputs(M, 4096, mode, True, xd) for _ in range(4)]
             def run():
                 for o in outs:  # each call reads the residual the previous one wrote
-                    gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
+                    if k > 1:
+                        gnq.gemma_add_rms_norm_quant_parts(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
+                    else:
+                        gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
             if graph:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g):
