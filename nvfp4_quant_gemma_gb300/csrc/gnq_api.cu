@@ -16,10 +16,10 @@ extern template cudaError_t launch_mode<MODE_NVFP4>(const Params &, int, bool,
                                                     const LaunchShape &, cudaStream_t);
 extern template cudaError_t launch_mode<MODE_MXFP8>(const Params &, int, bool,
                                                     const LaunchShape &, cudaStream_t);
-extern template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, bool, int, size_t);
-extern template int stream_blocks_per_sm<MODE_FP8>(int, bool, int, bool, int, size_t);
-extern template int stream_blocks_per_sm<MODE_NVFP4>(int, bool, int, bool, int, size_t);
-extern template int stream_blocks_per_sm<MODE_MXFP8>(int, bool, int, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, bool, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_FP8>(int, bool, int, bool, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_NVFP4>(int, bool, int, bool, bool, int, size_t);
+extern template int stream_blocks_per_sm<MODE_MXFP8>(int, bool, int, bool, bool, int, size_t);
 
 namespace {
 
@@ -87,23 +87,26 @@ bool row_shape_fits(int64_t H, int mode, int cluster, int vpt) {
     return threads <= max_threads(false, vpt);
 }
 
-int stream_occupancy_query(int mode, int dtype, bool parts, int vpt, bool lean, int threads,
-                           size_t smem) {
+int stream_occupancy_query(int mode, int dtype, bool parts, int vpt, bool lean, bool full,
+                           int threads, size_t smem) {
     switch (mode) {
-        case MODE_NONE: return stream_blocks_per_sm<MODE_NONE>(dtype, parts, vpt, lean, threads, smem);
-        case MODE_FP8: return stream_blocks_per_sm<MODE_FP8>(dtype, parts, vpt, lean, threads, smem);
+        case MODE_NONE:
+            return stream_blocks_per_sm<MODE_NONE>(dtype, parts, vpt, lean, full, threads, smem);
+        case MODE_FP8:
+            return stream_blocks_per_sm<MODE_FP8>(dtype, parts, vpt, lean, full, threads, smem);
         case MODE_NVFP4:
-            return stream_blocks_per_sm<MODE_NVFP4>(dtype, parts, vpt, lean, threads, smem);
-        default: return stream_blocks_per_sm<MODE_MXFP8>(dtype, parts, vpt, lean, threads, smem);
+            return stream_blocks_per_sm<MODE_NVFP4>(dtype, parts, vpt, lean, full, threads, smem);
+        default:
+            return stream_blocks_per_sm<MODE_MXFP8>(dtype, parts, vpt, lean, full, threads, smem);
     }
 }
 
 // Occupancy answers are cached per (device, instance, threads, smem): the
 // query is a driver call, and the answer never changes for a device.
-int stream_occupancy(int mode, int dtype, bool parts, int vpt, bool lean, int threads,
+int stream_occupancy(int mode, int dtype, bool parts, int vpt, bool lean, bool full, int threads,
                      size_t smem) {
     struct Entry {
-        int dev, mode, dtype, parts, vpt, lean, threads;
+        int dev, mode, dtype, parts, vpt, lean, full, threads;
         size_t smem;
         int blocks;
     };
@@ -117,14 +120,16 @@ int stream_occupancy(int mode, int dtype, bool parts, int vpt, bool lean, int th
         for (int i = 0; i < n_cached; ++i) {
             const Entry &e = cache[i];
             if (e.dev == dev && e.mode == mode && e.dtype == dtype && e.parts == (int)parts &&
-                e.vpt == vpt && e.lean == (int)lean && e.threads == threads && e.smem == smem)
+                e.vpt == vpt && e.lean == (int)lean && e.full == (int)full && e.threads == threads &&
+                e.smem == smem)
                 return e.blocks;
         }
     }
-    const int blocks = stream_occupancy_query(mode, dtype, parts, vpt, lean, threads, smem);
+    const int blocks = stream_occupancy_query(mode, dtype, parts, vpt, lean, full, threads, smem);
     std::lock_guard<std::mutex> lock(mu);
     if (n_cached < 256)
-        cache[n_cached++] = Entry{dev, mode, dtype, (int)parts, vpt, (int)lean, threads, smem, blocks};
+        cache[n_cached++] =
+            Entry{dev, mode, dtype, (int)parts, vpt, (int)lean, (int)full, threads, smem, blocks};
     return blocks;
 }
 
@@ -138,6 +143,7 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     const int64_t threads = (H / unit_elems(mode) + vpt - 1) / vpt;
     if (threads > max_threads(true, vpt)) return false;
     const int64_t thr = (threads + 31) / 32 * 32;
+    const bool full = H == (int64_t)vpt * unit_elems(mode) * thr;
     const int64_t stage = (int64_t)nops * 2 * H;
     if (stage >= (1 << 20)) return false;  // mbarrier transaction count limit
     // fp32 bias + w table of the register-light form (see stream_kernel)
@@ -147,7 +153,8 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     for (int S = 4; S >= 2; --S) {
         const int64_t smem = smem_for(S);
         if (smem > d.smem_optin) continue;
-        const int blocks = stream_occupancy(mode, dtype, k > 1, vpt, lean, (int)thr, (size_t)smem);
+        const int blocks =
+            stream_occupancy(mode, dtype, k > 1, vpt, lean, full, (int)thr, (size_t)smem);
         if (blocks > best_blocks) {
             best_blocks = blocks;
             best_S = S;
@@ -164,6 +171,7 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
     ls.grid = M < wave ? M : wave;
     ls.pdl = g_pdl.load() != 0;
     ls.lean = lean;
+    ls.full = full;
     return true;
 }
 
@@ -186,7 +194,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
     const int ff = g_force_form.load();
     const int nops = k + (res ? 1 : 0);
-    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false};
+    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false, false};
     // The packed (lean) form is chosen where four units per thread would
     // otherwise cost occupancy -- except in the streaming FP8 / MXFP8 /
     // no-quant kernel, which is instruction-bound -- and needs the Gemma or
@@ -237,6 +245,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     }
     const int64_t threads = (H / ls.cluster / unit_elems(mode) + ls.vpt - 1) / ls.vpt;
     ls.threads = (int)((threads + 31) / 32 * 32);
+    ls.full = H / ls.cluster == (int64_t)ls.vpt * unit_elems(mode) * ls.threads;
     ls.grid = M * ls.cluster;
     ls.lean = lean_for(ls.vpt, false);
     return ls;

@@ -218,7 +218,9 @@ template <int MODE, int VPT, bool PARTS, bool LEAN> struct RowForm {
     static constexpr int maxnreg = PARTS ? cap : occ;
 };
 
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+// FULL: the launch guarantees every unit of the CTA's segment is in range
+// (segment = VPT units x threads), so no unit needs a check.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float &cta_ss,
                                          float *es_smem) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
@@ -237,7 +239,7 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int u = v * NT + t;
-        ok[v] = u < nunits;
+        ok[v] = FULL || u < nunits;
         col[v] = (int)rank * p.seg + u * E;
         lc[v] = PRED && !ok[v] ? (int)rank * p.seg : col[v];
     }
@@ -433,19 +435,20 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
 // FP8, MXFP8 and no-quant rows: the compiler's own register choice.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
     GNQ_ROW_SMEM
-    row_body<T, MODE, PARTS, VPT, LEAN>(p, warp_ss, cta_ss, es_smem);
+    row_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, warp_ss, cta_ss, es_smem);
 }
 
-// NVFP4 rows: the RowForm register budget.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+// NVFP4 rows: the RowForm register budget (out-of-range units are
+// predicated, so there is no FULL instance).
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __global__ void __launch_bounds__(1024 / VPT) __maxnreg__((RowForm<MODE, VPT, PARTS, LEAN>::maxnreg))
     row_kernel_nvfp4(const __grid_constant__ Params p) {
-    static_assert(MODE == MODE_NVFP4, "NVFP4 rows only");
+    static_assert(MODE == MODE_NVFP4 && !FULL, "NVFP4 rows only");
     GNQ_ROW_SMEM
-    row_body<T, MODE, PARTS, VPT, LEAN>(p, warp_ss, cta_ss, es_smem);
+    row_body<T, MODE, PARTS, VPT, LEAN, false>(p, warp_ss, cta_ss, es_smem);
 }
 #undef GNQ_ROW_SMEM
 
@@ -469,7 +472,8 @@ template <int MODE, int VPT, bool LEAN> struct StreamForm {
     static constexpr int maxnreg = VPT == 1 ? 64 : (smem_w && VPT <= 2 ? 80 : 128);
 };
 
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+// FULL: the launch guarantees the row is exactly VPT units x threads.
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, float (*warp_ss)[32],
                                             float *es_smem) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
@@ -523,7 +527,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
         const int u = v * NT + t;
-        ok[v] = u < nunits;
+        ok[v] = FULL || u < nunits;
         col[v] = u * E;
         lc[v] = PRED && !ok[v] ? 0 : col[v];
         sfc[v] = sf_col_offset(col[v]);
@@ -703,19 +707,19 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
 // FP8, MXFP8 and no-quant streaming: the compiler's own register choice.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN>(p, dsmem, warp_ss, es_smem);
+    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem);
 }
 
-// NVFP4 streaming: the StreamForm register budget.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+// NVFP4 streaming: the StreamForm register budget (no FULL instance).
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) __maxnreg__((StreamForm<MODE, VPT, LEAN>::maxnreg))
     stream_kernel_nvfp4(const __grid_constant__ Params p) {
-    static_assert(MODE == MODE_NVFP4, "NVFP4 streaming only");
+    static_assert(MODE == MODE_NVFP4 && !FULL, "NVFP4 streaming only");
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN>(p, dsmem, warp_ss, es_smem);
+    stream_body<T, MODE, PARTS, VPT, LEAN, false>(p, dsmem, warp_ss, es_smem);
 }
 #undef GNQ_STREAM_SMEM
 

@@ -19,6 +19,7 @@ struct LaunchShape {
     size_t smem;     // streaming kernel: dynamic shared memory bytes
     bool pdl;        // launch as a programmatic dependent of the preceding grid
     bool lean;       // packed h / w form (fewest registers) instead of fp32 (fewest instructions)
+    bool full;       // every unit of a CTA's segment in range (VPT x threads units)
 };
 
 template <int MODE>
@@ -28,7 +29,37 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
 // Resident CTAs per SM of the streaming kernel instance for this shape (0 on
 // error); opts the instance in to `smem` bytes of dynamic shared memory.
 template <int MODE>
-int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, int threads, size_t smem);
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
+                         size_t smem);
+
+#define GNQ_PICK_L(K, T, VPT, L, F)                                                   \
+    (parts ? (void (*)(const Params))K<T, MODE, true, VPT, L, F>                        \
+           : (void (*)(const Params))K<T, MODE, false, VPT, L, F>)
+#define GNQ_PICK(K, T, VPT, F) (lean ? GNQ_PICK_L(K, T, VPT, true, F) : GNQ_PICK_L(K, T, VPT, false, F))
+
+#define GNQ_PICK_VPT(K, T, F)                                                         \
+    (vpt == 1 ? GNQ_PICK(K, T, 1, F) : vpt == 2 ? GNQ_PICK(K, T, 2, F) : GNQ_PICK(K, T, 4, F))
+#define GNQ_PICK_T(K, F) (dtype == 0 ? GNQ_PICK_VPT(K, __nv_bfloat16, F) : GNQ_PICK_VPT(K, __half, F))
+
+// The kernel instance of a launch shape.  `full`: every unit of a CTA's
+// segment is in range; FP8 streaming then runs instances without per-unit
+// checks (2.7 % faster on the fp16 16384 x 8192 no-residual batch; the same
+// for the FP8 row kernel measured 4 % slower on the decode batch).
+template <int MODE>
+void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream, bool full))(const Params) {
+    if constexpr (MODE == MODE_NVFP4) {
+        return stream ? GNQ_PICK_T(stream_kernel_nvfp4, false) : GNQ_PICK_T(row_kernel_nvfp4, false);
+    } else if constexpr (MODE == MODE_FP8) {
+        if (stream) return full ? GNQ_PICK_T(stream_kernel, true) : GNQ_PICK_T(stream_kernel, false);
+        return GNQ_PICK_T(row_kernel, false);
+    } else {
+        return stream ? GNQ_PICK_T(stream_kernel, false) : GNQ_PICK_T(row_kernel, false);
+    }
+}
+
+template <int MODE>
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
+                         size_t smem);
 
 #define GNQ_PICK_L(K, T, VPT, L)                                              \
     (parts ? (void (*)(const Params))K<T, MODE, true, VPT, L>                  \
@@ -55,8 +86,9 @@ void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream))(cons
 }
 
 template <int MODE>
-int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, int threads, size_t smem) {
-    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, lean, true);
+int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
+                         size_t smem) {
+    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, lean, true, full);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
         cudaSuccess)
         return 0;
@@ -69,7 +101,7 @@ int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, int threads,
 template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream) {
-    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.lean, ls.stream);
+    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.lean, ls.stream, ls.full);
     if (ls.stream) {
         // opt in to the dynamic shared memory this launch needs (idempotent)
         const cudaError_t e = cudaFuncSetAttribute(
@@ -100,6 +132,7 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
 
+#undef GNQ_PICK_T
 #undef GNQ_PICK_VPT
 #undef GNQ_PICK
 #undef GNQ_PICK_L

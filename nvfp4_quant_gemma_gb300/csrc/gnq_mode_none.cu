@@ -4,5 +4,5 @@
 namespace gnq {
 template cudaError_t launch_mode<MODE_NONE>(const Params &, int, bool, const LaunchShape &,
                                            cudaStream_t);
-template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, bool, int, size_t);
+template int stream_blocks_per_sm<MODE_NONE>(int, bool, int, bool, bool, int, size_t);
 }  // namespace gnq
