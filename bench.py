@@ -36,7 +36,8 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from nvfp4_quant_gemma_gb300.workloads import HEADLINE, WORKLOADS, DTYPES, make_inputs  # noqa: E402
+from nvfp4_quant_gemma_gb300.workloads import (HEADLINE, SMALL_M, WORKLOADS, DTYPES,  # noqa: E402
+                                                all_workloads, make_inputs)
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s for add+GemmaRMSNorm+quant"
 FALLBACK_HBM_GBS = 6800.0
@@ -222,7 +223,10 @@ class Case:
     def step(self, i: int, stream=None):
         x, r, out = self.sets[i % self.n_sets]
         wl = self.wl
-        if wl.k > 1:
+        if wl.weight_bias == 0.0:
+            self.gnq.add_rms_norm_quant(x, r, self.w, self.eps, self.scale, wl.mode,
+                                        write_y=wl.write_y, out=out, stream=stream)
+        elif wl.k > 1:
             self.gnq.gemma_add_rms_norm_quant_parts(x, r, self.w, self.eps, self.scale, wl.mode,
                                                     write_y=wl.write_y, out=out, stream=stream)
         elif wl.mode == "none":
@@ -371,7 +375,8 @@ def cpu_baseline(wl, budget_s: float = 10.0):
     passes = 0
     t0 = time.perf_counter()
     while True:
-        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y,
+                                        weight_bias=wl.weight_bias)
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -397,7 +402,7 @@ def run_gnq(args, rank: int, world: int, barrier):
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
     peak, peak_kind = measured_peak()
 
-    wl = WORKLOADS[args.workload]
+    wl = all_workloads()[args.workload]
     case = Case(gnq, wl, dev, exact_inputs=True, l2_bytes=l2)
     g_warm = case.graph(max(args.warmup, 1))
     g_timed = case.graph(args.steps, start=args.warmup)
@@ -464,31 +469,73 @@ def run_gnq(args, rank: int, world: int, barrier):
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget)
     if world == 1 and not args.no_table:
         line["workloads"] = workload_table(gnq, dev, l2, peak)
+    if world == 1 and not args.no_sweep:
+        line["small_m_sweep"] = small_m_sweep(gnq, dev, l2, peak)
     return line
 
 
+def time_case(case, dev) -> tuple[float, int]:
+    """Microseconds per call of a workload case: a CUDA graph of n back-to-back
+    launches over its rotating sets, n sized for ~0.3 ms of work."""
+    probe = case.graph(max(2, case.n_sets))
+    probe.replay()
+    torch.cuda.synchronize(dev)
+    t = time_graph(probe, dev, case.n_sets) / case.n_sets
+    n = int(min(4000, max(20, 0.3e3 / max(t, 1e-4))))
+    g = case.graph(n)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    ms = time_graph(g, dev, n)
+    del probe, g
+    return ms / n * 1e3, n
+
+
 def workload_table(gnq, dev, l2, peak):
+    """Every workload: the five configurations and the further variants
+    (MXFP8, plain RMSNorm, norm only) at their shapes."""
     rows = []
-    for name, wl in WORKLOADS.items():
+    for name, wl in all_workloads().items():
         case = Case(gnq, wl, dev, exact_inputs=(wl.M * wl.H <= 2 ** 22), l2_bytes=l2)
-        probe = case.graph(max(2, case.n_sets))
-        probe.replay()
-        torch.cuda.synchronize(dev)
-        t = time_graph(probe, dev, case.n_sets) / case.n_sets
-        n = int(min(4000, max(20, 0.3e3 / max(t, 1e-4))))
-        g = case.graph(n)
-        g.replay()
-        torch.cuda.synchronize(dev)
-        ms = time_graph(g, dev, n)
-        per = ms / n
+        us, n = time_case(case, dev)
         b = wl.algorithmic_bytes()
-        gbs = b / (per / 1e3) / 1e9
-        rows.append({"workload": name, "us_per_call": round(per * 1e3, 3), "GB_s": round(gbs, 1),
-                     "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(wl.M / (per / 1e3)),
+        gbs = b / (us / 1e6) / 1e9
+        rows.append({"workload": name, "kind": "config" if name in WORKLOADS else "variant",
+                     "us_per_call": round(us, 3), "GB_s": round(gbs, 1),
+                     "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(wl.M / (us / 1e6)),
                      "bytes_per_call": b, "launches_timed": n, "sets": case.n_sets,
                      "dram_traffic_per_launch": recorded_traffic(name)})
-        del case, probe, g
+        del case
         torch.cuda.empty_cache()
+    return rows
+
+
+# launch shapes compared by the small-batch sweep: (label, kernel, cluster)
+SWEEP_SHAPES = (("auto", 0, 0), ("row_cluster2", 1, 2), ("row_cluster4", 1, 4), ("stream", 2, 0))
+
+
+def small_m_sweep(gnq, dev, l2, peak):
+    """Latency of the headline's shape (H = 4096 bf16, FP8, y, residual) for
+    M = 1 .. 1024: the automatic launch shape against split-row clusters of 2
+    and 4 CTAs (partial sums of squares exchanged through distributed shared
+    memory) and the persistent streaming grid."""
+    base = WORKLOADS[HEADLINE]
+    rows = []
+    try:
+        for M in SMALL_M:
+            wl = base.with_rows(M)
+            case = Case(gnq, wl, dev, exact_inputs=True, l2_bytes=l2)
+            row = {"M": M}
+            for label, kernel, cluster in SWEEP_SHAPES:
+                gnq.set_launch_policy(kernel, cluster, 0, 0)
+                us, _ = time_case(case, dev)
+                row[label + "_us"] = round(us, 3)
+            gnq.set_launch_policy(0, 0, 0, 0)
+            row["auto_GB_s"] = round(wl.algorithmic_bytes() / (row["auto_us"] / 1e6) / 1e9, 1)
+            rows.append(row)
+            del case
+            torch.cuda.empty_cache()
+    finally:
+        gnq.set_launch_policy(0, 0, 0, 0)
     return rows
 
 
@@ -505,7 +552,7 @@ def run_reference(args, rank: int):
     oracle.build()
     threads = os.cpu_count() or 1
     oracle.set_threads(threads)
-    wl = WORKLOADS[args.workload]
+    wl = all_workloads()[args.workload]
     bits = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
     mode = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4, "mxfp8": oracle.MODE_MXFP8,
             "none": oracle.MODE_NONE}[wl.mode]
@@ -515,7 +562,8 @@ def run_reference(args, rank: int):
     pin = make_inputs(probe)
     t0 = time.perf_counter()
     oracle.gemma_add_rms_norm_quant(bits(pin["x"]), None if pin["residual"] is None else bits(pin["residual"]),
-                                    bits(pin["weight"]), wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+                                    bits(pin["weight"]), wl.eps, wl.scale, mode, dc, write_y=wl.write_y,
+                                    weight_bias=wl.weight_bias)
     per_row = (time.perf_counter() - t0) / probe.M
     rows = int(max(1, min(wl.M, args.ref_budget / max(1, args.steps) / max(per_row, 1e-9))))
     sample = wl.with_rows(rows)
@@ -524,10 +572,12 @@ def run_reference(args, rank: int):
     r = None if inp["residual"] is None else bits(inp["residual"])
     w = bits(inp["weight"])
     for _ in range(args.warmup):
-        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y,
+                                        weight_bias=wl.weight_bias)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y)
+        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y,
+                                        weight_bias=wl.weight_bias)
     el = time.perf_counter() - t0
     value = sample.algorithmic_bytes() * args.steps / el / 1e9
     sample_txt = f"{rows} of {wl.M} rows of {wl.name} per step"
@@ -554,7 +604,7 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gnq", choices=["gnq", "reference"])
-    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(all_workloads()))
     ap.add_argument("--soak", type=float, default=0.6,
                     help="seconds of identical replays before and after the timed replay, "
                          "so the clock sampler sees the load")
@@ -563,6 +613,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-table", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the small-batch latency sweep")
     ap.add_argument("--policy", default="0,0,0,0",
                     help="forced launch shape kernel,cluster,vpt,form (0 = automatic)")
     args = ap.parse_args()

@@ -33,7 +33,7 @@ class Workload:
     H: int
     dtype: str          # "bf16" | "fp16"
     mode: str           # "fp8" | "nvfp4" | "mxfp8" | "none"
-    scale: float        # FP8 static scale, or NVFP4 global scale
+    scale: float        # FP8 static scale, or NVFP4 global scale (unused otherwise)
     write_y: bool
     residual: bool
     seed: int
@@ -45,6 +45,7 @@ class Workload:
     n_outliers: int = 0
     outlier_mult: float = 20.0
     eps: float = 1e-6
+    weight_bias: float = 1.0  # 1: Gemma norm (1 + w); 0: plain RMSNorm (w)
 
     def with_rows(self, M: int) -> "Workload":
         return dataclasses.replace(self, M=M)
@@ -91,8 +92,32 @@ WORKLOADS = {
     ]
 }
 
+# The method's further variants at the same shapes: the MXFP8 output (E4M3
+# values + one E8M0 scale per 32 elements, row-major), the plain RMSNorm
+# (weight bias 0) and the norm alone (y, no quantization).
+EXTRA_WORKLOADS = {
+    w.name: w for w in [
+        Workload("decode_m256_h4096_bf16_mxfp8_y", 256, 4096, "bf16", "mxfp8", 0.0,
+                 write_y=True, residual=True, seed=1, r_var=9.0, n_outliers=8),
+        Workload("prefill_m16384_h8192_fp16_mxfp8", 16384, 8192, "fp16", "mxfp8", 0.0,
+                 write_y=False, residual=True, seed=3, r_var=16.0),
+        Workload("prefill_m16384_h8192_fp16_nvfp4_plain", 16384, 8192, "fp16", "nvfp4", 84.0,
+                 write_y=False, residual=True, seed=3, r_var=16.0, weight_bias=0.0),
+        Workload("prefill_m16384_h8192_fp16_norm_y", 16384, 8192, "fp16", "none", 0.0,
+                 write_y=True, residual=True, seed=3, r_var=16.0),
+    ]
+}
+
 # The decode batch the headline throughput is quoted on.
 HEADLINE = "decode_m256_h4096_bf16_fp8_y"
+
+# Batch sizes of the small-batch latency sweep (on the headline's H, dtype
+# and mode).
+SMALL_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)
+
+
+def all_workloads() -> dict:
+    return {**WORKLOADS, **EXTRA_WORKLOADS}
 
 
 def outlier_channels(wl: Workload) -> torch.Tensor:

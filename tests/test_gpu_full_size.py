@@ -1,5 +1,6 @@
-"""Full-size parity: every workload configuration at its real size, launched
-exactly as bench.py launches it (automatic policy, same inputs recipe).
+"""Full-size parity: every workload (the five configurations and the MXFP8,
+plain-RMSNorm and norm-only variants) at its real size, launched exactly as
+bench.py launches it (automatic policy, same inputs recipe).
 
 * Sampled rows (first, last, a seeded random set) against the oracle: the
   updated residual bit for bit, y within one ulp, codes and scales bit for
@@ -7,7 +8,9 @@ exactly as bench.py launches it (automatic policy, same inputs recipe).
 * Whole-tensor properties from independent library arithmetic: the
   residual equals torch's correctly rounded 16-bit add everywhere; FP8
   codes equal torch's fp32 division + saturating cast of the GPU's y
-  everywhere; NVFP4 codes dequantize to within one code step of y.
+  everywhere; NVFP4 codes dequantize to within one code step of y; MXFP8
+  scales are the E8M0 exponents of the GPU's own block amax and its codes
+  torch's saturating cast of y over the exact power-of-two scale.
 * The configured write_y=False call gives the same codes as a write_y=True
   call on the same inputs.
 """
@@ -17,11 +20,12 @@ import torch
 
 import oracle
 from gnq_testutil import DTYPE_CODE, bits, u8, ulp_distance16, unpack_nibbles
-from nvfp4_quant_gemma_gb300.workloads import WORKLOADS, make_inputs
+from nvfp4_quant_gemma_gb300.workloads import all_workloads, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-OMODE = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4}
+OMODE = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4, "mxfp8": oracle.MODE_MXFP8,
+         "none": oracle.MODE_NONE}
 N_SAMPLE = 24
 
 
@@ -45,16 +49,20 @@ def _call(gnq, wl, x, r, w, s, write_y):
     out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, write_y, x)
     if wl.mode == "nvfp4":
         out[1].view(torch.uint8).fill_(0xA5)
-    if wl.k > 1:
+    if wl.weight_bias == 0.0:
+        gnq.add_rms_norm_quant(x, r, w, wl.eps, s, wl.mode, write_y=write_y, out=out)
+    elif wl.k > 1:
         gnq.gemma_add_rms_norm_quant_parts(x, r, w, wl.eps, s, wl.mode, write_y=write_y, out=out)
+    elif wl.mode == "none":
+        gnq.gemma_add_rms_norm(x, r, w, wl.eps, y=out[2])
     else:
         gnq.gemma_add_rms_norm_quant(x, r, w, wl.eps, s, wl.mode, write_y=write_y, out=out)
     return out
 
 
-@pytest.mark.parametrize("name", list(WORKLOADS))
+@pytest.mark.parametrize("name", list(all_workloads()))
 def test_workload_full_size(gnq, name):
-    wl = WORKLOADS[name]
+    wl = all_workloads()[name]
     dev = torch.device("cuda")
     inp = make_inputs(wl)
     x = inp["x"].to(dev)
@@ -66,12 +74,13 @@ def test_workload_full_size(gnq, name):
 
     # the configured call (as bench.py times it), then one that also writes y
     r_a = None if r0 is None else r0.to(dev)
-    q_a, bs_a, _ = _call(gnq, wl, x, r_a, w, s, wl.write_y)
+    q_a, bs_a, y_a = _call(gnq, wl, x, r_a, w, s, wl.write_y)
     r_b = None if r0 is None else r0.to(dev)
     q_b, bs_b, y_b = _call(gnq, wl, x, r_b, w, s, True)
     torch.cuda.synchronize()
-    assert torch.equal(q_a.view(torch.uint8), q_b.view(torch.uint8))
-    if bs_a is not None and om == oracle.MODE_NVFP4:
+    if om != oracle.MODE_NONE:
+        assert torch.equal(q_a.view(torch.uint8), q_b.view(torch.uint8))
+    if bs_a is not None and om in (oracle.MODE_NVFP4, oracle.MODE_MXFP8):
         assert torch.equal(bs_a.view(torch.uint8), bs_b.view(torch.uint8))
     assert gnq.read_device_error() == 0
 
@@ -95,7 +104,20 @@ def test_workload_full_size(gnq, name):
         ref_q = (y_b.float() / s).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
         assert torch.equal(q_b.view(torch.uint8), ref_q.view(torch.uint8))
         del ref_q
-    else:
+    elif om == oracle.MODE_MXFP8:
+        # E8M0 code = floor(log2(block amax)) - 8 + 127 clamped to [0, 254] (0 for
+        # an all-zero block); codes = saturating E4M3 of y / 2^(code - 127)
+        yb32 = y_b.float().reshape(wl.M, wl.H // 32, 32)
+        amax = yb32.abs().amax(dim=-1)
+        e = torch.frexp(amax).exponent - 1          # floor(log2(amax)) for amax > 0
+        want = torch.where(amax > 0, (e - 8 + 127).clamp(0, 254), torch.zeros_like(e))
+        got = bs_b.view(torch.uint8).reshape(wl.M, wl.H // 32).long()
+        assert torch.equal(got, want.long())
+        inv = torch.ldexp(torch.ones_like(amax), (127 - got).to(torch.int32))
+        ref_q = (yb32 * inv[..., None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+        assert torch.equal(q_b.view(torch.uint8), ref_q.view(torch.uint8).reshape(wl.M, wl.H))
+        del yb32, amax, e, want, got, inv, ref_q
+    elif om == oracle.MODE_NVFP4:
         # decode codes * sf / g and check |dequant - y| <= one code step
         M, H = wl.M, wl.H
         codes = torch.stack([q_b & 0xF, q_b >> 4], dim=-1).reshape(M, H).long()
@@ -123,13 +145,18 @@ def test_workload_full_size(gnq, name):
     rs = None if r0 is None else r0[rows]
     ref = oracle.gemma_add_rms_norm_quant(bits(xs), None if rs is None else bits(rs),
                                           bits(inp["weight"]), wl.eps, wl.scale, om, dc,
-                                          write_y=True)
+                                          write_y=True, weight_bias=wl.weight_bias)
     if r0 is not None:
         assert np.array_equal(bits(r_a[rows]), ref["residual"])
     gy = bits(y_b[rows])
     assert int(ulp_distance16(gy, ref["y"]).max()) <= 1
+    if om == oracle.MODE_NONE:
+        assert torch.equal(y_a, y_b)
+        return
     qo, bso = oracle.quantize_from_y(gy, wl.scale, om, dc)
     assert np.array_equal(u8(q_a[rows]), qo)
+    if om == oracle.MODE_MXFP8:
+        assert np.array_equal(u8(bs_a[rows]), bso)
     if om == oracle.MODE_NVFP4:
         Kp = wl.H // 16
         flat = u8(bs_a).reshape(-1)
