@@ -206,14 +206,15 @@ __device__ __forceinline__ float inv_rms(const Params &p, float tot) {
 // Register budget of an NVFP4 row instance (row_kernel_nvfp4; the other
 // modes leave the choice to the compiler, which an explicit budget, even
 // one equal to the launch bound's, was measured to change for the worse).
-// The forms the launch policy picks for one activation get four resident
-// CTAs at their thread counts (160 threads at four 16-byte chunks per
-// thread, 128 at eight); the others keep what 1024 / VPT threads allow.
+// The forms the launch policy picks for one activation: 80 registers at
+// four 16-byte chunks per thread (five resident CTAs of 160 threads; 64
+// spills), 128 at eight (four CTAs of 128); the others keep what 1024 / VPT
+// threads allow.
 template <int MODE, int VPT, bool PARTS, bool LEAN> struct RowForm {
     static constexpr int U = Unit<MODE>::U, chunks = VPT * U;
     static constexpr int cap = VPT == 1 ? 64 : VPT == 2 ? 128 : 255;
     static constexpr int occ = chunks <= 2 ? 64
-                               : chunks == 4 ? (U == 2 ? 96 : LEAN ? 64 : cap)
+                               : chunks == 4 ? (U == 2 ? 80 : LEAN ? 64 : cap)
                                              : (LEAN ? 128 : cap);
     static constexpr int maxnreg = PARTS ? cap : occ;
 };
