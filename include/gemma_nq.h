@@ -174,6 +174,23 @@ const char *gnq_status_string(int status);
 int gnq_set_launch_policy(int kernel, int cluster, int vpt, int form);
 
 /*
+ * The launch shape the automatic policy picks for a call on the current
+ * device, in the terms of gnq_set_launch_policy (a forced policy is not
+ * applied): *kernel 1 or 2, *cluster CTAs per row (0 for the streaming
+ * kernel), *vpt 1, 2 or 4, *form 1 (fp32) or 2 (packed).  The arguments
+ * describe the call: rows M >= 1, width H, k partial buffers (1: one
+ * activation), whether it has a residual and writes y, mode, dtype, and the
+ * weight bias (1 Gemma, 0 plain).  Forcing the returned shape reproduces
+ * the automatic launch, for instance to run a call that writes y with
+ * exactly the arithmetic of one that does not.  Returns GNQ_OK;
+ * GNQ_ERR_NULL, GNQ_ERR_DTYPE, GNQ_ERR_MODE or GNQ_ERR_SHAPE for arguments a
+ * call would reject; GNQ_ERR_CUDA without a usable device.
+ */
+int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y, int mode,
+                     int dtype, float weight_bias, int *kernel, int *cluster, int *vpt,
+                     int *form);
+
+/*
  * Programmatic dependent launch (on by default): each launch may start while
  * the preceding kernel on the stream drains, and waits inside the kernel
  * (griddepcontrol.wait) until that kernel's results are visible before its

@@ -15,6 +15,7 @@ from ._binding import (  # noqa: F401
     quantize_fp8_values,
     read_device_error,
     load,
+    query_launch,
     set_launch_policy,
     set_pdl,
     status_string,

@@ -48,6 +48,7 @@ def load() -> ctypes.CDLL:
             "gemma_add_rms_norm_quant_parts": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "add_rms_norm_quant": [P, I, i64, P, P, F, P, I, I, P, P, P, i64, i64, I, P],
             "gnq_set_launch_policy": [I, I, I, I],
+            "gnq_query_launch": [i64, i64, I, I, I, I, I, F, P, P, P, P],
             "gnq_read_device_error": [P, I],
             "gnq_set_pdl": [I],
             "gnq_quantize_fp8_values": [P, i64, P, P, P],
@@ -67,7 +68,7 @@ def load() -> ctypes.CDLL:
 EXPORTS = ("gemma_add_rms_norm", "gemma_add_rms_norm_quant", "gemma_add_rms_norm_quant_parts",
            "add_rms_norm_quant", "gnq_status_string", "gnq_set_launch_policy",
            "gnq_read_device_error", "gnq_set_pdl", "gnq_encode_e4m3_e2m1",
-           "gnq_quantize_fp8_values")
+           "gnq_quantize_fp8_values", "gnq_query_launch")
 
 
 def status_string(status: int) -> str:
@@ -203,6 +204,18 @@ def set_launch_policy(kernel: int = 0, cluster: int = 0, vpt: int = 0, form: int
     1 = fp32 (fewest instructions), 2 = packed (fewest registers)."""
     _check(load().gnq_set_launch_policy(int(kernel), int(cluster), int(vpt), int(form)),
            "gnq_set_launch_policy")
+
+
+def query_launch(M: int, H: int, mode, dtype: str = "bf16", k: int = 1, residual: bool = True,
+                 write_y: bool = False, weight_bias: float = 1.0) -> tuple[int, int, int, int]:
+    """The automatic launch shape of a call, as (kernel, cluster, vpt, form) in
+    set_launch_policy's terms; forcing it reproduces the automatic launch."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    dt = {"bf16": 0, "fp16": 1}[dtype] if isinstance(dtype, str) else _DTYPE[dtype]
+    _check(load().gnq_query_launch(int(M), int(H), int(k), int(bool(residual)), int(bool(write_y)),
+                                   _mode(mode), dt, float(weight_bias),
+                                   *[ctypes.byref(o) for o in out]), "gnq_query_launch")
+    return tuple(o.value for o in out)
 
 
 def set_pdl(enable: bool) -> None:

@@ -181,28 +181,27 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
 //   * one activation with a residual: one CTA per row at every M -- one
 //     unit per thread below ~SMs rows, else ~256 threads (FP8, MXFP8, no
 //     quant) or ~160 threads (NVFP4) per CTA;
-//   * no residual: one CTA per row up to 16 x SMs rows, then rows stream
-//     through persistent CTAs of four units per thread (~256 threads for
-//     FP8 at H = 8192, ~128 for NVFP4);
+//   * no residual: one CTA per row up to 16 x SMs rows, then -- unless y
+//     is written (norm only, or write_y), where the row kernel stays ahead --
+//     rows stream through persistent CTAs of four units per thread (~256
+//     threads for FP8 at H = 8192, ~128 for NVFP4), in the packed form;
 //   * k partials: streaming from 4 x SMs rows (~256 threads; FP8 / MXFP8 /
 //     no quant ~512 from 16 x SMs rows), one CTA per row below.
 // A row is split over a cluster only when it has more than 1024 units: on
 // these shapes the cluster barrier always cost more than the extra SMs
 // gave back.
+// `forced`: apply the shape forced by gnq_set_launch_policy (else the
+// automatic choice alone).
 LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, int k,
-                         bool res, float weight_bias) {
-    const int fk = g_force_kernel.load(), fc = g_force_cluster.load(), fv = g_force_vpt.load();
-    const int ff = g_force_form.load();
+                         bool res, bool write_y, float weight_bias, bool forced = true) {
+    const int fk = forced ? g_force_kernel.load() : 0, fc = forced ? g_force_cluster.load() : 0;
+    const int fv = forced ? g_force_vpt.load() : 0, ff = forced ? g_force_form.load() : 0;
     const int nops = k + (res ? 1 : 0);
     LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false, false};
     // The packed (lean) form is chosen where four units per thread would
-    // otherwise cost occupancy -- except in the streaming FP8 / MXFP8 /
-    // no-quant kernel, which is instruction-bound -- and needs the Gemma or
-    // plain weight bias.
+    // otherwise cost occupancy; it needs the Gemma or plain weight bias.
     const bool lean_ok = weight_bias == 1.f || weight_bias == 0.f;
-    auto lean_for = [&](int v, bool stream) {
-        return lean_ok && (ff ? ff == 2 : v == 4 && !(stream && mode != MODE_NVFP4));
-    };
+    auto lean_for = [&](int v) { return lean_ok && (ff ? ff == 2 : v == 4); };
     const int64_t units = H / unit_elems(mode);
     auto vpt_for = [&](int64_t target) {
         int v = 1;
@@ -218,15 +217,15 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     } else if (res) {
         vpt = M < sms ? 1 : vpt_for(mode == MODE_NVFP4 ? 160 : 256);
     } else {
-        stream = M >= 16 * sms;
+        stream = M >= 16 * sms && !write_y;
         vpt = M < sms ? 1 : vpt_for(stream && mode == MODE_NVFP4 ? 128 : 256);
     }
     if (fk) stream = fk == 2;
     if (fv) vpt = fv;
-    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt, true), ls))
+    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls))
         return ls;
     if (stream &&
-        stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256), true), ls))
+        stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256)), ls))
         return ls;
 
     ls.vpt = fv ? fv : (stream ? 1 : vpt);
@@ -247,7 +246,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     ls.threads = (int)((threads + 31) / 32 * 32);
     ls.full = H / ls.cluster == (int64_t)ls.vpt * unit_elems(mode) * ls.threads;
     ls.grid = M * ls.cluster;
-    ls.lean = lean_for(ls.vpt, false);
+    ls.lean = lean_for(ls.vpt);
     return ls;
 }
 
@@ -299,7 +298,8 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 
     const DevInfo *d = dev_info();
     if (!d) return GNQ_ERR_CUDA;
-    const LaunchShape ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, weight_bias);
+    const LaunchShape ls =
+        choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias);
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
@@ -412,6 +412,29 @@ int gnq_set_launch_policy(int kernel, int cluster, int vpt, int form) {
     gnq::g_force_cluster.store(cluster);
     gnq::g_force_vpt.store(vpt);
     gnq::g_force_form.store(form);
+    return GNQ_OK;
+}
+
+int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y, int mode,
+                     int dtype, float weight_bias, int *kernel, int *cluster, int *vpt,
+                     int *form) {
+    if (!kernel || !cluster || !vpt || !form) return GNQ_ERR_NULL;
+    if (dtype != GNQ_BF16 && dtype != GNQ_FP16) return GNQ_ERR_DTYPE;
+    if (mode < gnq::MODE_NONE || mode > gnq::MODE_MXFP8) return GNQ_ERR_MODE;
+    if (k < 1 || k > gnq::kMaxParts) return GNQ_ERR_MODE;
+    if (M < 1 || H <= 0 || H > gnq::kMaxH || H % 8 != 0) return GNQ_ERR_SHAPE;
+    if (mode == gnq::MODE_NVFP4 && H % 64 != 0) return GNQ_ERR_SHAPE;
+    if (mode == gnq::MODE_MXFP8 && H % 32 != 0) return GNQ_ERR_SHAPE;
+    if (M > (int64_t)0x7FFFFFFF / 8) return GNQ_ERR_SHAPE;
+    const gnq::DevInfo *d = gnq::dev_info();
+    if (!d) return GNQ_ERR_CUDA;
+    const gnq::LaunchShape ls =
+        gnq::choose_shape(*d, M, H, mode, dtype, k, has_residual != 0,
+                          write_y != 0 || mode == gnq::MODE_NONE, weight_bias, false);
+    *kernel = ls.stream ? 2 : 1;
+    *cluster = ls.stream ? 0 : ls.cluster;
+    *vpt = ls.vpt;
+    *form = ls.lean ? 2 : 1;
     return GNQ_OK;
 }
 

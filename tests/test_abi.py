@@ -92,6 +92,28 @@ def test_parts_validation(lib):
     assert lib.gnq_read_device_error(None, 0) == 1
 
 
+def test_query_launch_validation(lib):
+    """gnq_query_launch rejects what a call would reject (before any device
+    query), and fails with GNQ_ERR_CUDA only for a valid call."""
+    q = lib.gnq_query_launch
+    outs = [ctypes.c_int(0) for _ in range(4)]
+    ptrs = [ctypes.byref(o) for o in outs]
+    i64, f = ctypes.c_int64, ctypes.c_float
+
+    def call(M=256, H=4096, k=1, res=1, wy=1, mode=0, dt=0, bias=1.0, p=ptrs):
+        return q(i64(M), i64(H), k, res, wy, mode, dt, f(bias), *p)
+
+    assert call(p=[None] + ptrs[1:]) == 1      # NULL output
+    assert call(dt=2) == 3                     # dtype
+    assert call(mode=3) == 4                   # mode
+    assert call(k=9) == 4                      # partial count
+    assert call(M=0) == 2                      # rows
+    assert call(H=100) == 2                    # H % 8
+    assert call(mode=1, H=96) == 2             # NVFP4 H % 64
+    assert call(H=65544) == 2                  # H too large
+    assert call() in (0, 7)                    # valid: a shape, or no device here
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     from nvfp4_quant_gemma_gb300 import _binding, build
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))

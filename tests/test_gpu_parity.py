@@ -292,10 +292,34 @@ def test_fp8_clamped_path_with_huge_weights(gnq, kernel):
         run_case(gnq, x, r, w, "fp8", 0.001, write_y=True, dtype="bf16")
 
 
-def test_automatic_policy_large_batch(gnq):
-    """The automatic choice for a prefill-sized batch (streaming kernel)."""
-    x, r, w = _make(2048, 5120, "bf16", seed=77)
-    run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
+@pytest.mark.parametrize("M,H,res,write_y,mode,scale,kernel", [
+    (2048, 5120, True, True, "nvfp4", 168.0, 1),    # residual: one CTA per row
+    (2560, 2048, False, False, "fp8", 0.05, 2),     # no residual, no y: streaming
+    (2560, 2048, False, False, "nvfp4", 168.0, 2),
+    (2560, 2048, False, False, "mxfp8", 0.0, 2),
+    (2560, 2048, False, True, "fp8", 0.05, 1),      # no residual, y written: one CTA per row
+])
+def test_automatic_policy_large_batch(gnq, M, H, res, write_y, mode, scale, kernel):
+    """The automatic launch shape of prefill-sized batches in each branch of
+    the policy (from 16 x SMs rows): the kernel it picks, and parity of the
+    automatic launch (a call without y in the shape the query reports for
+    it, compared with a call that writes y in that same shape)."""
+    x, r, w = _make(M, H, "bf16", seed=77)
+    shape = gnq.query_launch(M, H, mode, "bf16", residual=res, write_y=write_y)
+    if torch.cuda.get_device_properties(0).multi_processor_count * 16 <= M:
+        assert shape[0] == kernel
+        if shape[2] == 4:
+            assert shape[3] == 2  # packed form at four units per thread
+    if write_y:
+        run_case(gnq, x, r if res else None, w, mode, scale, write_y=True, dtype="bf16")
+    else:
+        # the automatic shape of the call without y, forced on both of
+        # run_case's calls (with and without y) so they share its arithmetic
+        gnq.set_launch_policy(*shape)
+        try:
+            run_case(gnq, x, r if res else None, w, mode, scale, write_y=False, dtype="bf16")
+        finally:
+            gnq.set_launch_policy(0, 0, 0, 0)
     assert gnq.read_device_error() == 0
 
 
