@@ -247,7 +247,8 @@ static void quant_row_nvfp4(const float *yf, int64_t m, int64_t H, float g,
 /* MXFP8 (OCP microscaling): per block of 32 elements, the shared scale is
  * X = 2^(floor(log2(amax)) - 8), 8 being the exponent of E4M3's largest
  * binade; it is stored as the E8M0 code floor(log2(amax)) - 8 + 127, clamped
- * to [0, 254] (an all-zero block gets code 0).  Elements are
+ * to [0, 254] (an all-zero block gets code 0; an infinite amax, whose
+ * floor(log2) is +inf, the top code 254).  Elements are
  * e4m3_satfinite(y / X), exact scaling by a power of two.  Scales are stored
  * row-major, (M, H/32). */
 static void quant_row_mxfp8(const float *yf, int64_t H, uint8_t *q,
@@ -259,6 +260,8 @@ static void quant_row_mxfp8(const float *yf, int64_t H, uint8_t *q,
         int code;
         if (amax == 0.0) {
             code = 0;
+        } else if (isinf(amax)) {
+            code = 254;
         } else {
             int e2;
             frexp(amax, &e2);

@@ -325,6 +325,24 @@ def test_mxfp8_scales_and_codes_from_library_arithmetic(oracle_lib):
     assert np.array_equal(q, ref.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
 
 
+def test_mxfp8_infinite_block_takes_the_top_code(oracle_lib):
+    """A block whose amax is inf (y overflowed): floor(log2(inf)) = +inf
+    clamps to code 254, X = 2^127; inf saturates to 448, finite values
+    divided by 2^127 fall below E4M3's smallest subnormal and keep their
+    sign (0x00 / 0x80).  The next block is unaffected."""
+    y = torch.zeros(1, 64, dtype=torch.bfloat16)
+    y[0, 3] = float("inf")
+    y[0, 5] = -2.0
+    y[0, 40] = 3.0
+    q, bs = oracle.quantize_from_y(bits(y), 0.0, oracle.MODE_MXFP8, oracle.BF16)
+    assert bs[0, 0] == 254
+    assert bs[0, 1] == 1 - 8 + 127           # floor(log2(3)) = 1
+    assert q[0, 3] == 0x7E                   # +448
+    assert q[0, 5] == 0x80                   # -2 / 2^127 -> -0
+    assert q[0, 0] == 0x00
+    assert q[0, 40] == 0x7C                  # 3 / 2^(1-8) = 384 = 1.5 * 2^8: exponent field 15, mantissa 100
+
+
 def test_quantize_from_y_agrees_with_full_pipeline(oracle_lib):
     M, H = 7, 512
     x = _rand((M, H), 1.0, "bf16", 17)
