@@ -242,6 +242,28 @@ template <> __device__ __forceinline__ uint32_t absmax16x2<__half>(uint32_t a, u
     asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
 }
+// max |v| over the 8 values of one packed chunk, as fp32 (exact; NaN lanes
+// drop out, as in fmax).
+template <typename T> __device__ __forceinline__ float absmax8(uint4 a) {
+    const uint32_t m = absmax16x2<T>(absmax16x2<T>(a.x, a.y), absmax16x2<T>(a.z, a.w));
+    float lo, hi;
+    Act<T>::unpack2(m, lo, hi);
+    return fmaxf(fabsf(lo), fabsf(hi));
+}
+
+// MXFP8 scale of a block amax (>= 0, or inf): the E8M0 code
+// floor(log2(amax)) - 8 + 127 clamped to [0, 254] -- read off the fp32
+// exponent field e: e - 8 for a normal amax, 0 for zero and subnormals
+// (their floor(log2) is at most -127), 254 for inf -- and the exact
+// multiplier 2^(127 - code) that divides the block by the scale.
+__device__ __forceinline__ uint32_t e8m0_code(float amax) {
+    const uint32_t e = __float_as_uint(amax) >> 23;
+    return e == 255u ? 254u : (e > 8u ? e - 8u : 0u);
+}
+__device__ __forceinline__ float e8m0_inverse(uint32_t code) {
+    return code == 254u ? 0x1p-127f : __uint_as_float((254u - code) << 23);
+}
+
 // max |v| over the 16 values of two packed chunks, as fp32 (exact).
 template <typename T> __device__ __forceinline__ float absmax16(uint4 a, uint4 b) {
     const uint32_t m = absmax16x2<T>(

@@ -11,15 +11,22 @@
 //
 // Two kernels share one per-unit epilogue (y, quantization, stores):
 //
-//   row_kernel     one CTA -- or a thread-block cluster of C CTAs meeting
-//                  through distributed shared memory -- per row, inputs
-//                  loaded straight into registers.  For small batches, where
-//                  splitting rows over clusters puts more SMs on HBM.
+//   row_kernel     one CTA per row -- or, for rows wider than 1024 units, a
+//                  thread-block cluster of C CTAs meeting through distributed
+//                  shared memory -- with the inputs loaded straight into
+//                  registers.  Every batch with one activation and a
+//                  residual, every batch below 16 x SMs rows, and batches
+//                  that write y.
 //   stream_kernel  persistent CTAs, each walking rows blockIdx.x, +grid, ...
 //                  The inputs of the next `stages` rows stream into a shared
 //                  memory ring by 1-D bulk copies completed on mbarriers, so
 //                  DRAM latency hides behind the arithmetic of earlier rows.
-//                  For large batches.
+//                  Large batches without a residual, and k partials.
+//
+// Each exists as two __global__ wrappers around one inlined body: the
+// FP8 / MXFP8 / no-quant instances (register choice left to the compiler)
+// and the *_nvfp4 instances (explicit register budgets, RowForm and
+// StreamForm).
 //
 // Work inside a CTA: a thread owns VPT units of U contiguous 16-byte chunks
 // (8U elements; U = 2 for NVFP4, so a thread holds whole 16-element blocks,
@@ -169,19 +176,17 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         st_v2_unit<true>(o.q + (col >> 1), lo, hi, ok);
         st_u8_unit<true>(o.sf + sfc, sf, ok);
     } else if (MODE == MODE_MXFP8) {
-        Act<T>::unpack(yb[0], yf);
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yf[i]));
+        // a 32-element block is the units of four consecutive lanes
+        float amax = absmax8<T>(yb[0]);
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));  // 32-element block
-        int code = 0;
-        if (amax > 0.f) code = min(max(ilogbf(amax) - 8 + 127, 0), 254);
-        mul_arr_s<8>(yf, ldexpf(1.0f, 127 - code));  // y / 2^(code-127), exact
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t code = e8m0_code(amax);
+        Act<T>::unpack(yb[0], yf);
+        mul_arr_s<8>(yf, e8m0_inverse(code));  // y / 2^(code-127), exact
         const uint32_t lo = e4m3x4(yf[0], yf[1], yf[2], yf[3]);
         const uint32_t hi = e4m3x4(yf[4], yf[5], yf[6], yf[7]);
         st_v2_unit<false>(o.q + col, lo, hi, ok);
-        st_u8_unit<false>(o.sf + (col >> 5), (uint32_t)code, ok && (t & 3) == 0);
+        st_u8_unit<false>(o.sf + (col >> 5), code, ok && (t & 3) == 0);
     }
 }
 

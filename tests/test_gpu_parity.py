@@ -292,6 +292,21 @@ def test_fp8_clamped_path_with_huge_weights(gnq, kernel):
         run_case(gnq, x, r, w, "fp8", 0.001, write_y=True, dtype="bf16")
 
 
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_mxfp8_overflowing_blocks(gnq, kernel, dtype):
+    """Weights that push y past the 16-bit range (fp16: inf; bf16: huge
+    finite values): blocks holding an inf take the top E8M0 code, the rest
+    of the row its own codes, exactly as the oracle quantizes the GPU's y."""
+    M, H = 300, 1024
+    x, r, w = _make(M, H, dtype, seed=43)
+    w = w.float()
+    w[5:37:3] = 6.0e4 if dtype == "fp16" else 1e38
+    w = w.to(DTYPES[dtype])
+    with forced_policy(gnq, kernel):
+        run_case(gnq, x, r, w, "mxfp8", 0.0, write_y=True, dtype=dtype)
+
+
 @pytest.mark.parametrize("M,H,res,write_y,mode,scale,kernel", [
     (2048, 5120, True, True, "nvfp4", 168.0, 1),    # residual: one CTA per row
     (2560, 2048, False, False, "fp8", 0.05, 2),     # no residual, no y: streaming

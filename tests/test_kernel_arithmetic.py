@@ -85,3 +85,36 @@ def test_single_rounding_alone_is_not_enough():
     vals = magnitudes("fp16")[::37]
     off = sum(rn32(Fraction(float(v)) * r6) != rn32(Fraction(float(v)) / 6) for v in vals)
     assert off > len(vals) // 10
+
+
+# --- MXFP8: the E8M0 scale code read off the exponent field -------------------
+#
+# The kernel takes code = floor(log2(amax)) - 8 + 127 clamped to [0, 254]
+# from the fp32 exponent field e of amax: e - 8 if e > 8, 0 below (zero and
+# subnormals), 254 for inf; and divides by the scale with the exact
+# multiplier 2^(127 - code), built as the fp32 pattern (254 - code) << 23
+# (2^-127, a subnormal, for code 254).
+
+def _kernel_code(amax: np.ndarray) -> np.ndarray:
+    e = amax.astype(np.float32).view(np.uint32) >> 23
+    return np.where(e == 255, 254, np.where(e > 8, e.astype(np.int64) - 8, 0))
+
+
+def _definition_code(amax: np.ndarray) -> np.ndarray:
+    a = amax.astype(np.float64)
+    _, e2 = np.frexp(np.where(np.isinf(a), 1.0, a))
+    code = np.clip(e2 - 1 - 8 + 127, 0, 254)
+    return np.where(a == 0, 0, np.where(np.isinf(a), 254, code))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_e8m0_code_from_exponent_field(dtype):
+    vals = np.concatenate([[0.0], magnitudes(dtype), [np.inf]]).astype(np.float32)
+    assert np.array_equal(_kernel_code(vals), _definition_code(vals))
+
+
+def test_e8m0_inverse_is_the_exact_power_of_two():
+    for code in range(255):
+        bits = 0x00400000 if code == 254 else (254 - code) << 23
+        got = np.array([bits], dtype=np.uint32).view(np.float32)[0]
+        assert Fraction(float(got)) == Fraction(2) ** (127 - code)
