@@ -27,8 +27,13 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - All tensor pointers are DEVICE pointers on the current CUDA device, in
- *    row-major contiguous layout.  Activations x, residual, y and the weight
+ *  - All tensor pointers are addresses the current CUDA device can access,
+ *    in row-major contiguous layout: device memory, or pinned host memory
+ *    (mapped into the device's address space; on a Grace-Blackwell node the
+ *    kernels then read and write it over NVLink-C2C, with no separate copy).
+ *    A call whose activations are in host memory always runs one CTA per
+ *    row (plain loads and stores), never the streaming kernel, whose bulk
+ *    copies read device memory.  Activations x, residual, y and the weight
  *    w are 16-bit, of the type named by `dtype` (GNQ_BF16 or GNQ_FP16).
  *  - The caller owns and allocates every buffer.  The library allocates
  *    nothing per call and keeps no state other than cached device properties.

@@ -3,7 +3,8 @@
 Every step of the operation runs in the library's CUDA kernels; this module
 checks tensor metadata, allocates outputs with PyTorch the way
 "vllm.models.qwen3_5.nvidia.ops.fused_norm_quant" (gemma_add_rms_norm_quant)
-does, passes raw device pointers and the current CUDA stream through ctypes,
+does, passes raw pointers (CUDA or pinned host memory) and the current CUDA
+stream through ctypes,
 and turns a nonzero status into an exception.  There is no fallback: if the
 library is missing, every call raises.
 """
@@ -98,9 +99,14 @@ def _mode(mode) -> int:
     return int(mode)
 
 
+def _reachable(t: torch.Tensor) -> bool:
+    """A tensor the GPU can address: CUDA memory or pinned (mapped) host memory."""
+    return t.is_cuda or t.is_pinned()
+
+
 def _check_act(x: torch.Tensor, name: str) -> None:
-    if not x.is_cuda or not x.is_contiguous() or x.dtype not in _DTYPE:
-        raise ValueError(f"{name} must be a contiguous CUDA bf16/fp16 tensor")
+    if not _reachable(x) or not x.is_contiguous() or x.dtype not in _DTYPE:
+        raise ValueError(f"{name} must be a contiguous bf16/fp16 tensor in CUDA or pinned memory")
 
 
 def round_up(a: int, b: int) -> int:
@@ -109,20 +115,21 @@ def round_up(a: int, b: int) -> int:
 
 def alloc_outputs(M: int, H: int, mode, write_y: bool, like: torch.Tensor):
     """(q, block_scale, y) buffers as the pages allocate them; block_scale is
-    None for FP8 (whose block scale is the static scale tensor)."""
+    None for FP8 (whose block scale is the static scale tensor).  Placed like
+    `like`: on its CUDA device, or in pinned host memory for a host tensor."""
     m = _mode(mode)
-    dev = like.device
+    kw = {"device": like.device} if like.is_cuda else {"pin_memory": True}
     q = bs = None
     if m in (0, 2):
-        q = torch.empty((M, H), dtype=torch.float8_e4m3fn, device=dev)
+        q = torch.empty((M, H), dtype=torch.float8_e4m3fn, **kw)
     elif m == 1:
-        q = torch.empty((M, H // 2), dtype=torch.uint8, device=dev)
+        q = torch.empty((M, H // 2), dtype=torch.uint8, **kw)
     if m == 1:
         bs = torch.empty((round_up(M, 128), round_up(H // 16, 4) // 4), dtype=torch.int32,
-                         device=dev).view(torch.float8_e4m3fn)
+                         **kw).view(torch.float8_e4m3fn)
     elif m == 2:
-        bs = torch.empty((M, H // 32), dtype=torch.uint8, device=dev)
-    y = torch.empty((M, H), dtype=like.dtype, device=dev) if (write_y or m == -1) else None
+        bs = torch.empty((M, H // 32), dtype=torch.uint8, **kw)
+    y = torch.empty((M, H), dtype=like.dtype, **kw) if (write_y or m == -1) else None
     return q, bs, y
 
 
@@ -132,7 +139,7 @@ def gemma_add_rms_norm(x, residual, weight, eps, y=None, stream=None):
     _check_act(x, "x")
     M, H = x.shape
     if y is None:
-        y = torch.empty_like(x)
+        y = torch.empty_like(x) if x.is_cuda else torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     st = load().gemma_add_rms_norm(_ptr(x), _ptr(residual), _ptr(weight), float(eps), _ptr(y),
                                    M, H, _DTYPE[x.dtype], _stream(stream))
     _check(st, "gemma_add_rms_norm")
@@ -142,8 +149,8 @@ def gemma_add_rms_norm(x, residual, weight, eps, y=None, stream=None):
 def _scale_ptr(scale):
     if scale is None:
         return None
-    if not (scale.is_cuda and scale.dtype == torch.float32 and scale.numel() == 1):
-        raise ValueError("scale must be a 1-element fp32 CUDA tensor")
+    if not (_reachable(scale) and scale.dtype == torch.float32 and scale.numel() == 1):
+        raise ValueError("scale must be a 1-element fp32 tensor in CUDA or pinned memory")
     return _ptr(scale)
 
 
@@ -170,8 +177,9 @@ def gemma_add_rms_norm_quant(x, residual, weight, eps, scale, nvfp4=False, write
 def _parts_call(fn_name, x_parts, residual, weight, eps, scale, mode, write_y, out, stream):
     if x_parts.dim() == 2:
         x_parts = x_parts.unsqueeze(0)
-    if not x_parts.is_cuda or not x_parts.is_contiguous() or x_parts.dtype not in _DTYPE:
-        raise ValueError("x_parts must be a contiguous CUDA bf16/fp16 tensor (k, M, H)")
+    if not _reachable(x_parts) or not x_parts.is_contiguous() or x_parts.dtype not in _DTYPE:
+        raise ValueError("x_parts must be a contiguous bf16/fp16 tensor (k, M, H) in CUDA or "
+                         "pinned memory")
     k, M, H = x_parts.shape
     m = _mode(mode)
     q, bs, y = out if out is not None else alloc_outputs(M, H, m, write_y, x_parts)

@@ -133,6 +133,17 @@ int stream_occupancy(int mode, int dtype, bool parts, int vpt, bool lean, bool f
     return blocks;
 }
 
+// True if `ptr` is host memory (pinned and mapped into the device's address
+// space); unregistered or device memory gives false.
+bool in_host_memory(const void *ptr) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();  // clear the error of an unregistered pointer
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
 // Streaming kernel shape.  For each ring depth S (rows in flight per CTA,
 // 2..4) the occupancy calculator gives the resident CTAs per SM of this
 // instance; the shape with the most resident threads wins (ties: deeper
@@ -193,7 +204,8 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
 // `forced`: apply the shape forced by gnq_set_launch_policy (else the
 // automatic choice alone).
 LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, int k,
-                         bool res, bool write_y, float weight_bias, bool forced = true) {
+                         bool res, bool write_y, float weight_bias, bool forced = true,
+                         bool allow_stream = true) {
     const int fk = forced ? g_force_kernel.load() : 0, fc = forced ? g_force_cluster.load() : 0;
     const int fv = forced ? g_force_vpt.load() : 0, ff = forced ? g_force_form.load() : 0;
     const int nops = k + (res ? 1 : 0);
@@ -221,6 +233,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
         vpt = M < sms ? 1 : vpt_for(stream && mode == MODE_NVFP4 ? 128 : 256);
     }
     if (fk) stream = fk == 2;
+    if (!allow_stream) stream = false;
     if (fv) vpt = fv;
     if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls))
         return ls;
@@ -298,8 +311,14 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 
     const DevInfo *d = dev_info();
     if (!d) return GNQ_ERR_CUDA;
-    const LaunchShape ls =
+    LaunchShape ls =
         choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias);
+    // The streaming kernel's bulk copies read device memory; activations in
+    // host memory (mapped pinned memory, read over the host link) run on the
+    // row kernel, whose plain loads and stores reach any mapped address.
+    if (ls.stream && (in_host_memory(x) || (residual && in_host_memory(residual))))
+        ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias,
+                          true, false);
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;

@@ -505,3 +505,37 @@ def test_status_codes_with_device_buffers(gnq):
     assert call(P(x), P(r), P(w), 1e-6, P(s), 9, 0, P(q), None, None, 4, 128, 0, None) == 4
     torch.cuda.synchronize()
     assert torch.count_nonzero(r) == 0  # rejected calls had no effect
+
+
+@pytest.mark.parametrize("M,H,mode,scale,res,write_y", [
+    (256, 4096, "fp8", 0.05, True, True),      # the decode batch: one CTA per row
+    (40, 5120, "nvfp4", 168.0, True, True),
+    (3000, 2048, "fp8", 0.05, False, False),   # would stream on device: host input keeps rows
+])
+def test_pinned_host_buffers(gnq, M, H, mode, scale, res, write_y):
+    """Every buffer in pinned host memory (read and written by the kernels
+    through the host link, no copy): the same bits as the device buffers."""
+    x, r, w = _make(M, H, "bf16", seed=47)
+    r = r if res else None
+    s = torch.tensor([scale], dtype=torch.float32)
+    outs = {}
+    for where in ("cuda", "host"):
+        def place(t):
+            if t is None:
+                return None
+            return t.to("cuda") if where == "cuda" else t.clone().pin_memory()
+        xd, rd, wd, sd = place(x), place(r), place(w), place(s)
+        out = gnq.alloc_outputs(M, H, mode, write_y, xd)
+        if mode == "nvfp4":
+            out[1].view(torch.uint8).fill_(0xA5)
+        # host activations always take the row kernel; run the device side
+        # in it too, so both sum the squares in the same order
+        with forced_policy(gnq, 1 if where == "cuda" else 0):
+            gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=write_y, out=out)
+        torch.cuda.synchronize()
+        outs[where] = [t.cpu().view(torch.uint8) if t.dtype != torch.bfloat16 else t.cpu()
+                       for t in out if t is not None] + ([rd.cpu()] if rd is not None else [])
+        if where == "host":
+            assert all(t.is_pinned() for t in out if t is not None)
+    assert all(torch.equal(a, b) for a, b in zip(outs["cuda"], outs["host"]))
+    assert gnq.read_device_error() == 0
