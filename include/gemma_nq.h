@@ -31,9 +31,9 @@
  *    in row-major contiguous layout: device memory, or pinned host memory
  *    (mapped into the device's address space; on a Grace-Blackwell node the
  *    kernels then read and write it over NVLink-C2C, with no separate copy).
- *    A call whose activations are in host memory always runs one CTA per
- *    row (plain loads and stores), never the streaming kernel, whose bulk
- *    copies read device memory.  Activations x, residual, y and the weight
+ *    A call whose activations are not in device memory always runs one CTA
+ *    per row (plain loads and stores), never the streaming kernel, whose
+ *    bulk copies read device memory.  Activations x, residual, y and the weight
  *    w are 16-bit, of the type named by `dtype` (GNQ_BF16 or GNQ_FP16).
  *  - The caller owns and allocates every buffer.  The library allocates
  *    nothing per call and keeps no state other than cached device properties.
@@ -180,8 +180,8 @@ int gnq_set_launch_policy(int kernel, int cluster, int vpt, int form);
 
 /*
  * The launch shape the automatic policy picks for a call on the current
- * device, in the terms of gnq_set_launch_policy (a forced policy is not
- * applied): *kernel 1 or 2, *cluster CTAs per row (0 for the streaming
+ * device with its activations in device memory, in the terms of
+ * gnq_set_launch_policy (a forced policy is not applied): *kernel 1 or 2, *cluster CTAs per row (0 for the streaming
  * kernel), *vpt 1, 2 or 4, *form 1 (fp32) or 2 (packed).  The arguments
  * describe the call: rows M >= 1, width H, k partial buffers (1: one
  * activation), whether it has a residual and writes y, mode, dtype, and the

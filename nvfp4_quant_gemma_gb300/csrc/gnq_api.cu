@@ -133,15 +133,16 @@ int stream_occupancy(int mode, int dtype, bool parts, int vpt, bool lean, bool f
     return blocks;
 }
 
-// True if `ptr` is host memory (pinned and mapped into the device's address
-// space); unregistered or device memory gives false.
-bool in_host_memory(const void *ptr) {
+// True if `ptr` is plain device memory: the only memory the streaming
+// kernel's bulk copies are given.  Pinned host memory, managed memory and
+// anything the runtime does not know (or fails to classify) give false.
+bool in_device_memory(const void *ptr) {
     cudaPointerAttributes a;
     if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
-        cudaGetLastError();  // clear the error of an unregistered pointer
+        cudaGetLastError();  // clear the error, so it is not reported by the launch
         return false;
     }
-    return a.type == cudaMemoryTypeHost;
+    return a.type == cudaMemoryTypeDevice;
 }
 
 // Streaming kernel shape.  For each ring depth S (rows in flight per CTA,
@@ -313,10 +314,11 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     if (!d) return GNQ_ERR_CUDA;
     LaunchShape ls =
         choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias);
-    // The streaming kernel's bulk copies read device memory; activations in
-    // host memory (mapped pinned memory, read over the host link) run on the
-    // row kernel, whose plain loads and stores reach any mapped address.
-    if (ls.stream && (in_host_memory(x) || (residual && in_host_memory(residual))))
+    // The streaming kernel's bulk copies read device memory; activations
+    // anywhere else (mapped pinned host memory, read over the host link) run
+    // on the row kernel, whose plain loads and stores reach any address the
+    // device can access.
+    if (ls.stream && (!in_device_memory(x) || (residual && !in_device_memory(residual))))
         ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias,
                           true, false);
     p.seg = (int)(H / ls.cluster);
