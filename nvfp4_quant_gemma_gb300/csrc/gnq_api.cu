@@ -29,7 +29,6 @@ constexpr int kMaxParts = 8;
 
 struct DevInfo {
     int sms;
-    int smem_per_sm;    // bytes of shared memory per SM
     int smem_optin;     // largest dynamic shared memory a CTA may opt in to
     unsigned int *err;  // device address of the error word
 };
@@ -55,8 +54,6 @@ const DevInfo *dev_info() {
     if (g_ready[dev].load(std::memory_order_acquire) == 0) {
         DevInfo d{};
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
-                                   dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
                                    dev) != cudaSuccess ||
             cudaGetSymbolAddress(reinterpret_cast<void **>(&d.err), g_device_error) !=
