@@ -427,15 +427,33 @@ def e2e_zero_copy(gnq, wl, dev, steps: int, warmup: int, l2_bytes: int, barrier=
     return e0.elapsed_time(e1), h2d, d2h
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.strip().lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith(("model name", "cpu part")):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(wl, budget_s: float = 10.0):
     """The oracle as it stands, on the host cores, over repeated passes of a
-    row sample of the workload for about budget_s seconds."""
+    row sample of the workload: about budget_s seconds with OpenMP over rows
+    on every core, then about budget_s / 4 on one thread."""
     import numpy as np
 
     import oracle
     oracle.build()
     threads = os.cpu_count() or 1
-    oracle.set_threads(threads)
     rows = min(wl.M, 256)
     sample = wl.with_rows(rows)
     inp = make_inputs(sample)
@@ -446,19 +464,29 @@ def cpu_baseline(wl, budget_s: float = 10.0):
     mode = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4, "mxfp8": oracle.MODE_MXFP8,
             "none": oracle.MODE_NONE}[wl.mode]
     dc = 0 if wl.dtype == "bf16" else 1
-    passes = 0
-    t0 = time.perf_counter()
-    while True:
-        oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc, write_y=wl.write_y,
-                                        weight_bias=wl.weight_bias)
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
-    gbs = sample.algorithmic_bytes() * passes / el / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+
+    def timed(n_threads, budget):
+        oracle.set_threads(n_threads)
+        passes = 0
+        t0 = time.perf_counter()
+        while True:
+            oracle.gemma_add_rms_norm_quant(x, r, w, wl.eps, wl.scale, mode, dc,
+                                            write_y=wl.write_y, weight_bias=wl.weight_bias)
+            passes += 1
+            el = time.perf_counter() - t0
+            if el >= budget:
+                return passes, el
+
+    passes, el = timed(threads, budget_s)
+    passes1, el1 = timed(1, budget_s / 4)
+    oracle.set_threads(threads)
+    per_pass = sample.algorithmic_bytes() / 1e9
+    return {"value": per_pass * passes / el, "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{passes} passes over {rows} rows of {wl.name} ({el:.1f} s)",
-            "tokens_per_s": rows * passes / el}
+            "tokens_per_s": rows * passes / el,
+            "single_thread_value": per_pass * passes1 / el1,
+            "single_thread_sample": f"{passes1} passes ({el1:.1f} s, 1 thread)",
+            "cpu_model": cpu_model()}
 
 
 def run_gnq(args, rank: int, world: int, barrier):
@@ -672,7 +700,7 @@ def run_reference(args, rank: int):
         "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "io_dtype": wl.dtype,
                    "mode": wl.mode, "sample": sample_txt},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": sample_txt},
+                         "kind": "oracle", "sample": sample_txt, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
