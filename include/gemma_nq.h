@@ -72,7 +72,9 @@ typedef enum {
     GNQ_ERR_MODE = 4,  /* unknown quantization mode, or k out of range      */
     GNQ_ERR_ALIAS = 5, /* x == residual, or y aliases x or residual         */
     GNQ_ERR_ALIGN = 6, /* a pointer or the partial stride is misaligned     */
-    GNQ_ERR_CUDA = 7   /* the CUDA runtime reported an error at launch      */
+    GNQ_ERR_CUDA = 7   /* the CUDA runtime reported an error at launch (the
+                          runtime's last-error state is cleared, so the
+                          caller's own later checks do not see it)         */
 } gnq_status;
 
 typedef enum { GNQ_BF16 = 0, GNQ_FP16 = 1 } gnq_dtype;

@@ -331,7 +331,9 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
         case MODE_NVFP4: e = launch_mode<MODE_NVFP4>(p, dtype, parts, ls, s); break;
         default: e = launch_mode<MODE_MXFP8>(p, dtype, parts, ls, s); break;
     }
-    return e == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
+    if (e == cudaSuccess) return GNQ_OK;
+    cudaGetLastError();  // reported here; do not leave it for the caller's next check
+    return GNQ_ERR_CUDA;
 }
 
 // Groups of 8 values through the kernels' FP8 encoder: the paired path
