@@ -446,7 +446,7 @@ template <int PATH>
 __device__ __forceinline__ void fp8_codes8(const float *y, const Fp8Div &d, uint32_t &lo,
                                            uint32_t &hi) {
     float q[8];
-    if (PATH == FP8_PAIR) {
+    if constexpr (PATH == FP8_PAIR) {
         const uint64_t nr = pk2(-d.r, -d.r), s2 = pk2(d.s, d.s);
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
@@ -457,12 +457,12 @@ __device__ __forceinline__ void fp8_codes8(const float *y, const Fp8Div &d, uint
         }
         lo = e4m3x4(q[0], q[1], q[2], q[3]) ^ 0x80808080u;
         hi = e4m3x4(q[4], q[5], q[6], q[7]) ^ 0x80808080u;
-        return;
-    }
+    } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(y[i], d.s);
-    lo = e4m3x4(q[0], q[1], q[2], q[3]);
-    hi = e4m3x4(q[4], q[5], q[6], q[7]);
+        for (int i = 0; i < 8; ++i) q[i] = __fdiv_rn(y[i], d.s);
+        lo = e4m3x4(q[0], q[1], q[2], q[3]);
+        hi = e4m3x4(q[4], q[5], q[6], q[7]);
+    }
 }
 
 // amax / 6 correctly rounded, for amax the magnitude of a 16-bit value (0,

@@ -59,34 +59,6 @@ void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream, bool 
 
 template <int MODE>
 int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
-                         size_t smem);
-
-#define GNQ_PICK_L(K, T, VPT, L)                                              \
-    (parts ? (void (*)(const Params))K<T, MODE, true, VPT, L>                  \
-           : (void (*)(const Params))K<T, MODE, false, VPT, L>)
-#define GNQ_PICK(K, T, VPT) (lean ? GNQ_PICK_L(K, T, VPT, true) : GNQ_PICK_L(K, T, VPT, false))
-
-#define GNQ_PICK_VPT(K, T)                                                    \
-    (vpt == 1 ? GNQ_PICK(K, T, 1) : vpt == 2 ? GNQ_PICK(K, T, 2) : GNQ_PICK(K, T, 4))
-
-template <int MODE>
-void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream))(const Params) {
-    if constexpr (MODE == MODE_NVFP4) {
-        if (stream)
-            return dtype == 0 ? GNQ_PICK_VPT(stream_kernel_nvfp4, __nv_bfloat16)
-                              : GNQ_PICK_VPT(stream_kernel_nvfp4, __half);
-        return dtype == 0 ? GNQ_PICK_VPT(row_kernel_nvfp4, __nv_bfloat16)
-                          : GNQ_PICK_VPT(row_kernel_nvfp4, __half);
-    } else {
-        if (stream)
-            return dtype == 0 ? GNQ_PICK_VPT(stream_kernel, __nv_bfloat16)
-                              : GNQ_PICK_VPT(stream_kernel, __half);
-        return dtype == 0 ? GNQ_PICK_VPT(row_kernel, __nv_bfloat16) : GNQ_PICK_VPT(row_kernel, __half);
-    }
-}
-
-template <int MODE>
-int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
                          size_t smem) {
     void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, lean, true, full);
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
