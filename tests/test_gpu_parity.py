@@ -293,6 +293,24 @@ def test_fp8_clamped_path_with_huge_weights(gnq, kernel):
 
 
 @pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_extreme_scales(gnq, kernel, dtype):
+    """The fused kernels at the edges of their scale handling: static FP8
+    scales at and beyond the FMA-corrected quotient's range [2^-80, 2^80]
+    (outside it, and for a negative scale, the kernels divide), and NVFP4
+    global scales across the fp32 range (block scales saturating at 448,
+    subnormal, or zero so every code is a signed zero)."""
+    M, H = 70, 1024
+    x, r, w = _make(M, H, dtype, seed=53)
+    with forced_policy(gnq, kernel):
+        for s in (2.0 ** -90, 2.0 ** -80, 2.0 ** 80, 2.0 ** 81, 1e30, -0.05):
+            run_case(gnq, x, r, w, "fp8", s, write_y=True, dtype=dtype)
+        for g in (2.0 ** -60, 1e-6, 1.0, 1e6, 2.0 ** 100):
+            run_case(gnq, x, r, w, "nvfp4", g, write_y=False, dtype=dtype)
+    assert gnq.read_device_error() == 0
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
 @pytest.mark.parametrize("dtype", ["fp16", "bf16"])
 def test_mxfp8_overflowing_blocks(gnq, kernel, dtype):
     """Weights that push y past the 16-bit range (fp16: inf; bf16: huge

@@ -34,6 +34,12 @@ MUTATIONS = [
     ("e2m1_no_explicit_saturation", "if (a >= 6.0) return sign | 0x7;", "if (isinf(a)) return sign | 0x7;"),
     ("bf16_truncates", "double n = rint(a / ulp);", "double n = floor(a / ulp);"),
     ("mx_scale_off_by_one", "code = (e2 - 1) - 8 + 127;", "code = e2 - 8 + 127;"),
+    ("mx_infinite_block_code_zero", "} else if (isinf(amax)) {\n            code = 254;",
+     "} else if (isinf(amax)) {\n            code = 0;"),
+    ("mx_elements_unscaled", "or_e4m3_encode((double)yf[32 * b + j] / X)",
+     "or_e4m3_encode((double)yf[32 * b + j])"),
+    ("swizzle_tile_row_stride", "(m / 128) * (Kp / 4) + k / 4", "(m / 128) * Kp + k / 4"),
+    ("swizzle_tile_col_stride", "(m / 128) * (Kp / 4) + k / 4", "(m / 128) * (Kp / 4) + k / 2"),
 ]
 
 
