@@ -109,6 +109,42 @@ def _check_act(x: torch.Tensor, name: str) -> None:
         raise ValueError(f"{name} must be a contiguous bf16/fp16 tensor in CUDA or pinned memory")
 
 
+def _check_buf(t, name: str, nbytes: int, dtype=None, required: bool = True) -> None:
+    """A buffer the kernels read or write: contiguous, of `dtype` if given, at
+    least `nbytes` long, in CUDA or pinned memory.  Raises before any launch
+    (the library itself cannot see a buffer's size)."""
+    if t is None:
+        if required:
+            raise ValueError(f"{name} is required here")
+        return
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * t.element_size()} bytes; the call needs {nbytes}")
+    if not _reachable(t):
+        raise ValueError(f"{name} must be in CUDA or pinned host memory")
+
+
+def _check_call(M: int, H: int, k: int, dt, residual, weight, mode: int, write_y: bool, out):
+    """Sizes of every buffer a call touches (x itself checked by the caller)."""
+    e = 2
+    _check_buf(residual, "residual", M * H * e, dt, required=False)
+    _check_buf(weight, "weight", H * e, dt)
+    q, bs, y = out
+    if mode in (0, 2):
+        _check_buf(q, "q", M * H)
+    elif mode == 1:
+        _check_buf(q, "q", M * H // 2)
+    if mode == 1:
+        _check_buf(bs, "block_scale", round_up(M, 128) * round_up(H // 16, 4))
+    elif mode == 2:
+        _check_buf(bs, "block_scale", M * (H // 32))
+    if write_y or mode == -1:
+        _check_buf(y, "y", M * H * e, dt)
+
+
 def round_up(a: int, b: int) -> int:
     return (a + b - 1) // b * b
 
@@ -140,6 +176,7 @@ def gemma_add_rms_norm(x, residual, weight, eps, y=None, stream=None):
     M, H = x.shape
     if y is None:
         y = torch.empty_like(x) if x.is_cuda else torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    _check_call(M, H, 1, x.dtype, residual, weight, -1, True, (None, None, y))
     st = load().gemma_add_rms_norm(_ptr(x), _ptr(residual), _ptr(weight), float(eps), _ptr(y),
                                    M, H, _DTYPE[x.dtype], _stream(stream))
     _check(st, "gemma_add_rms_norm")
@@ -167,6 +204,7 @@ def gemma_add_rms_norm_quant(x, residual, weight, eps, scale, nvfp4=False, write
     M, H = x.shape
     m = _mode(nvfp4)
     q, bs, y = out if out is not None else alloc_outputs(M, H, m, write_y, x)
+    _check_call(M, H, 1, x.dtype, residual, weight, m, write_y, (q, bs, y))
     st = load().gemma_add_rms_norm_quant(
         _ptr(x), _ptr(residual), _ptr(weight), float(eps), _scale_ptr(scale), m,
         1 if write_y else 0, _ptr(q), _ptr(bs), _ptr(y), M, H, _DTYPE[x.dtype], _stream(stream))
@@ -183,6 +221,7 @@ def _parts_call(fn_name, x_parts, residual, weight, eps, scale, mode, write_y, o
     k, M, H = x_parts.shape
     m = _mode(mode)
     q, bs, y = out if out is not None else alloc_outputs(M, H, m, write_y, x_parts)
+    _check_call(M, H, k, x_parts.dtype, residual, weight, m, write_y, (q, bs, y))
     st = getattr(load(), fn_name)(
         _ptr(x_parts), k, M * H, _ptr(residual), _ptr(weight), float(eps), _scale_ptr(scale), m,
         1 if (write_y or m == -1) else 0, _ptr(q), _ptr(bs), _ptr(y), M, H,

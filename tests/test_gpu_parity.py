@@ -557,3 +557,41 @@ def test_pinned_host_buffers(gnq, M, H, mode, scale, res, write_y):
             assert all(t.is_pinned() for t in out if t is not None)
     assert all(torch.equal(a, b) for a, b in zip(outs["cuda"], outs["host"]))
     assert gnq.read_device_error() == 0
+
+
+def test_binding_rejects_bad_buffers(gnq):
+    """The binding checks every buffer's size, dtype, layout and placement
+    before it launches anything (the C ABI cannot see a buffer's size), so
+    a short or mistyped buffer raises instead of being written past."""
+    dev = torch.device("cuda")
+    M, H = 8, 256
+    x = torch.randn(M, H, device=dev).to(torch.bfloat16)
+    r = torch.randn(M, H, device=dev).to(torch.bfloat16)
+    w = torch.randn(H, device=dev).to(torch.bfloat16)
+    s = torch.tensor([168.0], device=dev)
+    q, bs, y = gnq.alloc_outputs(M, H, "nvfp4", True, x)
+    r0 = r.clone()
+    bad = [
+        dict(out=(q[:-1], bs, y)),                                   # q one row short
+        dict(out=(q, bs.view(torch.uint8)[:-1], y)),                 # scale padding missing
+        dict(out=(q, bs, y.float())),                                # y of the wrong dtype
+        dict(out=(q, bs, y.t().contiguous().t())),                   # y not contiguous
+        dict(out=(q, bs, None)),                                     # y missing with write_y
+        dict(weight=w.float()),                                      # weight of the wrong dtype
+        dict(weight=w[: H // 2]),                                    # weight too short
+        dict(residual=r[: M // 2]),                                  # residual too short
+        dict(residual=r.cpu()),                                      # pageable host memory
+    ]
+    for case in bad:
+        kw = dict(out=(q, bs, y), weight=w, residual=r)
+        kw.update(case)
+        with pytest.raises(ValueError):
+            gnq.gemma_add_rms_norm_quant(x, kw["residual"], kw["weight"], 1e-6, s, "nvfp4",
+                                         write_y=True, out=kw["out"])
+    torch.cuda.synchronize()
+    assert torch.equal(r, r0)  # nothing ran
+    with pytest.raises(ValueError):
+        gnq.gemma_add_rms_norm(x, r, w, 1e-6, y=y[: M // 2])
+    with pytest.raises(ValueError):
+        gnq.gemma_add_rms_norm_quant_parts(torch.stack([x, x]), r, w, 1e-6, s, "fp8",
+                                           out=(q, None, None))              # q sized for NVFP4
