@@ -54,6 +54,9 @@
  *    exist) and MXFP8 H % 32 == 0.  H is at most 65536.
  *  - x and residual must not be the same buffer, and y must differ from both
  *    (GNQ_ERR_ALIAS).
+ *  - Every buffer must hold at least the elements its shape below states;
+ *    the library receives raw pointers and cannot check sizes (the Python
+ *    binding does, before any launch).
  */
 #ifndef GEMMA_NQ_H
 #define GEMMA_NQ_H
