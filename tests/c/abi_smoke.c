@@ -86,6 +86,27 @@ int main(void) {
         return fail("empty batch");
     unsigned int flags = 1;
     if (gnq_read_device_error(&flags, 1) != GNQ_OK || flags != 0) return fail("device error word");
+
+    /* the automatic launch shape, and forcing it reproduces the same bits */
+    int kernel = 0, cluster = -1, vpt = 0, form = 0;
+    if (gnq_query_launch(M, H, 1, 1, 1, GNQ_FP8, GNQ_BF16, 1.0f, &kernel, &cluster, &vpt, &form) !=
+        GNQ_OK)
+        return fail("query launch");
+    if (kernel != 1 || vpt < 1 || vpt > 4 || (form != 1 && form != 2))
+        return fail("query launch values");  /* three rows: one CTA per row */
+    if (gnq_query_launch(M, H, 1, 1, 1, GNQ_FP8, GNQ_BF16, 1.0f, NULL, &cluster, &vpt, &form) !=
+        GNQ_ERR_NULL)
+        return fail("query launch NULL status");
+    cudaMemcpy(r, hr, sizeof hr, cudaMemcpyHostToDevice);
+    if (gnq_set_launch_policy(kernel, cluster, vpt, form) != GNQ_OK) return fail("set policy");
+    st = gemma_add_rms_norm_quant(x, r, w, 1e-6f, s, GNQ_FP8, 1, q, NULL, y, M, H, GNQ_BF16, NULL);
+    gnq_set_launch_policy(0, 0, 0, 0);
+    if (st != GNQ_OK) return fail(gnq_status_string(st));
+    if (cudaDeviceSynchronize() != cudaSuccess) return fail("sync");
+    cudaMemcpy(out_q, q, sizeof out_q, cudaMemcpyDeviceToHost);
+    for (int i = 0; i < M * H; ++i)
+        if (out_q[i] != 0x64) return fail("forced shape: fp8 code != 0x64");
+    if (strlen(gnq_status_string(GNQ_ERR_ALIGN)) == 0) return fail("status string");
     printf("c abi ok\n");
     return 0;
 }
