@@ -63,6 +63,26 @@ def test_nvfp4_block_golden(oracle_lib):
         assert bs.reshape(-1)[oracle.swizzle_offset(0, b, 4)] == 0
 
 
+def test_mxfp8_row_example(oracle_lib):
+    """Hand-worked MXFP8 row (tests/golden/mxfp8_block_example.txt): scale
+    codes from floor(log2(amax)), an E4M3 tie, subnormal codes and a
+    half-subnormal tie, an all-zero block, saturation."""
+    d = _golden("mxfp8_block_example.txt")
+    y = np.zeros((1, 128))
+    for b in range(4):
+        vals = [float(v) for v in d.get(f"y{b}", [])]
+        y[0, 32 * b: 32 * b + len(vals)] = vals
+    yt = torch.tensor(y, dtype=torch.bfloat16)
+    assert torch.equal(yt.double(), torch.tensor(y))  # every listed value is a bf16
+    yt[0, 6] = -0.0                                     # block 0's signed zero
+    q, bs = oracle.quantize_from_y(bits(yt), 0.0, oracle.MODE_MXFP8, oracle.BF16)
+    for b in range(4):
+        assert bs[0, b] == int(d[f"code{b}"][0])
+        want = [int(v, 16) for v in d.get(f"q{b}", [])]
+        got = list(q[0, 32 * b: 32 * (b + 1)])
+        assert got[: len(want)] == want and all(c == 0 for c in got[len(want):])
+
+
 # --- residual add --------------------------------------------------------------
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
