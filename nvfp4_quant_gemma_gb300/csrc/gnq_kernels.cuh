@@ -136,8 +136,9 @@ template <bool PRED> __device__ __forceinline__ void st_u8_unit(void *p, uint32_
 // One unit of y (8U values before rounding): round, store y, quantize the
 // rounded values and store codes and scales.  `t` is the thread index;
 // FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA; `sfc` is the
-// unit's sf_col_offset (NVFP4).
-template <typename T, int MODE, int FP8PATH>
+// unit's sf_col_offset (NVFP4).  PRED: out-of-range units are predicated
+// (Pred<MODE>), unless the instance has none (FULL).
+template <typename T, int MODE, int FP8PATH, bool PRED = Pred<MODE>::value>
 __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &qc,
                                               float (&yf)[Unit<MODE>::E], const RowOut &o,
                                               int col, int sfc, bool ok, int t) {
@@ -146,8 +147,7 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
 #pragma unroll
     for (int c = 0; c < U; ++c) {
         yb[c] = pack8<T>(&yf[8 * c]);
-        if (Pred<MODE>::value ? p.write_y != 0 : p.write_y && ok)
-            st_v4_unit<Pred<MODE>::value>(o.y + col + 8 * c, yb[c], ok);
+        if (PRED ? p.write_y != 0 : p.write_y && ok) st_v4_unit<PRED>(o.y + col + 8 * c, yb[c], ok);
     }
 
     if (MODE == MODE_FP8) {
@@ -173,8 +173,8 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         mul_arr_s<16>(yf, qc.es_tab[sf]);
         const uint32_t lo = e2m1x8(&yf[0]);
         const uint32_t hi = e2m1x8(&yf[8]);
-        st_v2_unit<true>(o.q + (col >> 1), lo, hi, ok);
-        st_u8_unit<true>(o.sf + sfc, sf, ok);
+        st_v2_unit<PRED>(o.q + (col >> 1), lo, hi, ok);
+        st_u8_unit<PRED>(o.sf + sfc, sf, ok);
     } else if (MODE == MODE_MXFP8) {
         // a 32-element block is the units of four consecutive lanes
         float amax = absmax8<T>(yb[0]);
@@ -484,7 +484,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                                             float *es_smem) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     constexpr bool SW = StreamForm<MODE, VPT, LEAN>::smem_w;
-    constexpr bool PRED = Pred<MODE>::value;
+    constexpr bool PRED = Pred<MODE>::value && !FULL;  // FULL: no unit is out of range
 
     const int NT = blockDim.x;
     const int t = threadIdx.x;
@@ -695,7 +695,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                                  a[e], a[e + 1]);
                     }
                 }
-                epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
+                epilogue_unit<T, MODE, decltype(path)::value, PRED>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
             }
         };
         if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
@@ -719,13 +719,13 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __g
     stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem);
 }
 
-// NVFP4 streaming: the StreamForm register budget (no FULL instance).
+// NVFP4 streaming: the StreamForm register budget.
 template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) __maxnreg__((StreamForm<MODE, VPT, LEAN>::maxnreg))
     stream_kernel_nvfp4(const __grid_constant__ Params p) {
-    static_assert(MODE == MODE_NVFP4 && !FULL, "NVFP4 streaming only");
+    static_assert(MODE == MODE_NVFP4, "NVFP4 streaming only");
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN, false>(p, dsmem, warp_ss, es_smem);
+    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem);
 }
 #undef GNQ_STREAM_SMEM
 

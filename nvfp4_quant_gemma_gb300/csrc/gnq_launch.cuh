@@ -42,13 +42,19 @@ int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, i
 #define GNQ_PICK_T(K, F) (dtype == 0 ? GNQ_PICK_VPT(K, __nv_bfloat16, F) : GNQ_PICK_VPT(K, __half, F))
 
 // The kernel instance of a launch shape.  `full`: every unit of a CTA's
-// segment is in range; FP8 streaming then runs instances without per-unit
-// checks (2.7 % faster on the fp16 16384 x 8192 no-residual batch; the same
-// for the FP8 row kernel measured 4 % slower on the decode batch).
+// segment is in range; FP8 streaming, and NVFP4 streaming of one
+// activation, then run instances without per-unit checks (2.7 % and 3.0 %
+// faster on the fp16 16384 x 8192 no-residual batches; the same for the FP8
+// row kernel measured 4 % slower on the decode batch, for NVFP4 partials
+// 0.6 % slower).
 template <int MODE>
 void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream, bool full))(const Params) {
     if constexpr (MODE == MODE_NVFP4) {
-        return stream ? GNQ_PICK_T(stream_kernel_nvfp4, false) : GNQ_PICK_T(row_kernel_nvfp4, false);
+        // one activation only: with k partials the check-free instance was slower
+        if (stream)
+            return full && !parts ? GNQ_PICK_T(stream_kernel_nvfp4, true)
+                                  : GNQ_PICK_T(stream_kernel_nvfp4, false);
+        return GNQ_PICK_T(row_kernel_nvfp4, false);
     } else if constexpr (MODE == MODE_FP8) {
         if (stream) return full ? GNQ_PICK_T(stream_kernel, true) : GNQ_PICK_T(stream_kernel, false);
         return GNQ_PICK_T(row_kernel, false);
