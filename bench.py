@@ -1,16 +1,18 @@
 """Throughput of the fused add + Gemma RMSNorm + quant op on GB300.
 
-One step = one call of the op over one batch of the decode workload (M=256,
-H=4096, bf16, static FP8 with y and in-place residual); the per-workload
-table adds the prefill and tensor-parallel-partial shapes.  Prints ONE JSON
+One step = one call of the op over one batch of the largest workload (prefill,
+M=16384, H=8192, fp16, static FP8 with an in-place residual: 939.5 MB per
+call); the per-workload table adds the decode, M=2048 and
+tensor-parallel-partial shapes and the method's variants.  Prints ONE JSON
 line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gnq|reference]
 
 Timing: W untimed steps, then exactly K steps captured in one CUDA graph and
 timed with CUDA events on the capture stream, bracketed by a barrier and a
-device synchronize.  Every step reads a different input set; the sets
-together exceed twice the L2 size, so no step finds its inputs in L2.  Under
+device synchronize.  Every step reads a different input set; each step's
+inputs are larger than L2 and the sets together exceed twice the L2 size, so
+no step finds its inputs in L2.  Under
 torchrun every rank runs an independent replica (rows are independent, there
 is no data exchange); the slowest rank's time is reported and the value is
 the bytes all ranks moved over that time.
@@ -36,8 +38,9 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from nvfp4_quant_gemma_gb300.workloads import (HEADLINE, SMALL_M, WORKLOADS, DTYPES,  # noqa: E402
-                                                all_workloads, make_inputs)
+from nvfp4_quant_gemma_gb300.workloads import (HEADLINE, SMALL_M, SWEEP_BASES,  # noqa: E402
+                                                WORKLOADS, DTYPES, all_workloads, make_inputs,
+                                                sweep_workload)
 
 METRIC = "achieved HBM GB/s (% of GB300 peak) and tokens/s for add+GemmaRMSNorm+quant"
 FALLBACK_HBM_GBS = 6800.0
@@ -168,6 +171,43 @@ def device_uuid(dev: torch.device):
         return u if u.startswith("GPU-") else "GPU-" + u
     except Exception:
         return None
+
+
+def workload_config(wl, world: int) -> dict:
+    """The `config` object of a bench line: the workload alone, identical for
+    the GPU arm and the reference arm on the same workload."""
+    return {
+        "workload": wl.name, "M": wl.M, "H": wl.H, "io_dtype": wl.dtype, "mode": wl.mode,
+        "write_y": wl.write_y, "residual": wl.residual, "partials": wl.k,
+        "weight_bias": wl.weight_bias,
+        "parallelism": f"replicas{world}" if world > 1 else "single",
+        "l2": (f"inputs larger than L2: each step moves {wl.algorithmic_bytes() / 1e6:.1f} MB; "
+               "steps rotate over input/output sets that together exceed 2x L2"
+               if wl.algorithmic_bytes() > 128 * 2 ** 20 else
+               "steps rotate over input/output sets that together exceed 2x L2"),
+    }
+
+
+def kernel_name(kernel: int, cluster: int, vpt: int, form: int, wl) -> str:
+    """Readable name of the kernel instance a launch shape runs (the shape
+    as gnq_query_launch reports it)."""
+    base = "row_kernel" if kernel == 1 else "stream_kernel"
+    if wl.mode == "nvfp4":
+        base += "_nvfp4"
+    tname = {"bf16": "__nv_bfloat16", "fp16": "__half"}[wl.dtype]
+    mode = {"none": "MODE_NONE", "fp8": "MODE_FP8", "nvfp4": "MODE_NVFP4",
+            "mxfp8": "MODE_MXFP8"}[wl.mode]
+    name = (f"gnq::{base}<{tname}, {mode}, parts={'true' if wl.k > 1 else 'false'}, VPT={vpt}, "
+            f"{'packed' if form == 2 else 'fp32'}>")
+    if kernel == 1 and cluster > 1:
+        name += f" x {cluster}-CTA cluster"
+    return name
+
+
+def launched_kernel(gnq, wl) -> str:
+    shape = gnq.query_launch(wl.M, wl.H, wl.mode, wl.dtype, k=wl.k, residual=wl.residual,
+                             write_y=wl.write_y, weight_bias=wl.weight_bias)
+    return kernel_name(*shape, wl)
 
 
 # ----------------------------------------------------------------------------
@@ -427,6 +467,64 @@ def e2e_zero_copy(gnq, wl, dev, steps: int, warmup: int, l2_bytes: int, barrier=
     return e0.elapsed_time(e1), h2d, d2h
 
 
+def host_link(dev, nbytes: int = 1 << 30, reps: int = 5) -> dict:
+    """Copy-engine bandwidth between pinned host memory and the device:
+    host->device, device->host, and both directions at once on two streams
+    (best of `reps` copies of `nbytes`, CUDA events)."""
+    h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    d_b = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    s1, s2 = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def best(fn):
+        t = []
+        for _ in range(reps):
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            main = torch.cuda.current_stream(dev)
+            e0.record(main)
+            fn(main)
+            e1.record(main)
+            torch.cuda.synchronize(dev)
+            t.append(e0.elapsed_time(e1))
+        return min(t)
+
+    def h2d(main):
+        d_a.copy_(h_in, non_blocking=True)
+
+    def d2h(main):
+        h_out.copy_(d_b, non_blocking=True)
+
+    def both(main):
+        for st in (s1, s2):
+            st.wait_stream(main)
+        with torch.cuda.stream(s1):
+            d_a.copy_(h_in, non_blocking=True)
+        with torch.cuda.stream(s2):
+            h_out.copy_(d_b, non_blocking=True)
+        main.wait_stream(s1)
+        main.wait_stream(s2)
+
+    gbs = lambda ms, n: n / (ms / 1e3) / 1e9
+    out = {"h2d_GB_s": round(gbs(best(h2d), nbytes), 1),
+           "d2h_GB_s": round(gbs(best(d2h), nbytes), 1),
+           "bidirectional_GB_s": round(gbs(best(both), 2 * nbytes), 1),
+           "how": f"cudaMemcpyAsync of {nbytes >> 20} MiB between pinned host memory and the "
+                  f"device, best of {reps}; bidirectional: one copy each way on two streams"}
+    del h_in, h_out, d_a, d_b
+    return out
+
+
+def link_ceiling(bytes_step: int, h2d: int, d2h: int, link: dict) -> float:
+    """The end-to-end value the host link alone allows: a step's copies in
+    and out overlapped at the measured one-way and two-way rates."""
+    t_one = max(h2d / (link["h2d_GB_s"] * 1e9), d2h / (link["d2h_GB_s"] * 1e9))
+    t_two = (h2d + d2h) / (link["bidirectional_GB_s"] * 1e9)
+    return bytes_step / max(t_one, t_two) / 1e9
+
+
 def cpu_model() -> str:
     """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
     try:
@@ -517,25 +615,35 @@ def run_gnq(args, rank: int, world: int, barrier):
     value = bytes_step * args.steps * world / (ms_max / 1e3) / 1e9
     per_launch_s = ms / 1e3 / args.steps
     achieved = bytes_step / per_launch_s / 1e9
+    n_sets, footprint = case.n_sets, case.footprint
+    kernel = launched_kernel(gnq, wl) if args.policy == "0,0,0,0" else f"forced {args.policy}"
 
     e2e = None
     if not args.no_e2e:
         # end to end through the public API with host buffers
-        e2e_steps = max(1, min(args.steps, 500, int(4e9 // bytes_step)))
+        del case, g_warm, g_timed
+        torch.cuda.empty_cache()
+        e2e_steps = max(1, min(args.steps, 500, int(8e9 // bytes_step)))
         zc_ms, h2d, d2h = e2e_zero_copy(gnq, wl, dev, e2e_steps, 3, l2, barrier)
         cp_ms, _, _ = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier, graph=True)
         eager_ms, _, _ = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier, graph=False)
         gbs = lambda t: bytes_step * e2e_steps * world / (max_over_ranks(t, world, dev) / 1e3) / 1e9
-        e2e = {"value": round(gbs(zc_ms), 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        link = host_link(dev)
+        vals = {"direct": gbs(zc_ms), "copy_engine": gbs(cp_ms), "eager": gbs(eager_ms)}
+        e2e = {"value": round(vals["copy_engine"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-               "copy_engine_value": round(gbs(cp_ms), 2),
-               "eager_value": round(gbs(eager_ms), 2),
+               "direct_value": round(vals["direct"], 2),
+               "eager_value": round(vals["eager"], 2),
+               "host_link": link,
+               "link_ceiling_value": round(link_ceiling(bytes_step, h2d, d2h, link) * world, 2),
                "how": "every step's inputs come from pinned host memory and its results go back "
-                      "to pinned host memory, through the Python API. value: the kernels read "
-                      "and write the host buffers directly over the host link (no separate "
-                      "copy), steps replayed from a CUDA graph. copy_engine_value: explicit "
-                      "copies in and out on two streams around the same call, graph-replayed; "
-                      "eager_value: the same issued one call at a time from Python."}
+                      "to pinned host memory, through the Python API. value: explicit copies in "
+                      "and out on two streams around each call, the steps replayed from a CUDA "
+                      "graph. eager_value: the same issued one call at a time from Python. "
+                      "direct_value: the kernels read and write the host buffers over the host "
+                      "link themselves (no separate copy), graph-replayed. "
+                      "link_ceiling_value: the value the measured copy-engine rates of the host "
+                      "link allow for this step's bytes in and out."}
 
     if rank != 0:
         return None
@@ -553,23 +661,21 @@ def run_gnq(args, rank: int, world: int, barrier):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded normals; no dataset or weights involved)",
-        "config": {
-            "workload": wl.name, "M": wl.M, "H": wl.H, "io_dtype": wl.dtype, "mode": wl.mode,
-            "write_y": wl.write_y, "residual": wl.residual, "partials": wl.k,
-            "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": f"{case.n_sets} rotating input/output sets, {case.footprint / 1e6:.0f} MB "
-                  f"> 2x L2 ({l2 / 1e6:.0f} MB)",
-            "tokens_per_s": wl.M * args.steps * world / (ms_max / 1e3),
-            "us_per_call": ms_max / args.steps * 1e3,
-            "pct_of_peak": round(100 * achieved / peak, 1),
-            "timing": "K launches captured in one CUDA graph, CUDA events on the capture stream",
-        },
+        "config": workload_config(wl, world),
+        "tokens_per_s": wl.M * args.steps * world / (ms_max / 1e3),
+        "us_per_call": ms_max / args.steps * 1e3,
+        "pct_of_peak": round(100 * achieved / peak, 1),
+        "pct_of_nominal_8TBs": round(100 * achieved / 8000.0, 1),
+        "timing": (f"K launches captured in one CUDA graph over {n_sets} rotating input/output "
+                   f"sets ({footprint / 1e6:.0f} MB > 2x L2 of {l2 / 1e6:.0f} MB), CUDA events on "
+                   "the capture stream"),
         "roofline": {
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": traffic,
             "peak_kind": peak_kind,
             "algorithmic_bytes_per_launch": bytes_step,
-            "kernel": "gnq::row_kernel",
+            "kernel": kernel,
+            "traffic_source": "profiles/dram_traffic.txt (ncu, steady state)" if traffic else None,
         },
         "gpu_launches": args.steps,
     }
@@ -624,27 +730,30 @@ def workload_table(gnq, dev, l2, peak):
 SWEEP_SHAPES = (("auto", 0, 0), ("row_cluster2", 1, 2), ("row_cluster4", 1, 4), ("stream", 2, 0))
 
 
-def small_m_sweep(gnq, dev, l2, peak):
-    """Latency of the headline's shape (H = 4096 bf16, FP8, y, residual) for
-    M = 1 .. 1024: the automatic launch shape against split-row clusters of 2
-    and 4 CTAs (partial sums of squares exchanged through distributed shared
-    memory) and the persistent streaming grid."""
-    base = WORKLOADS[HEADLINE]
+def small_m_sweep(gnq, dev, l2, peak, modes=("fp8", "nvfp4"), m_values=SMALL_M):
+    """Latency for M = 1 .. 8192 rows at H = 5120 (bf16, residual, y), in the
+    static-FP8 and the NVFP4 mode: the automatic launch shape against
+    split-row clusters of 2 and 4 CTAs (partial sums of squares exchanged
+    through distributed shared memory) and the persistent streaming grid."""
     rows = []
     try:
-        for M in SMALL_M:
-            wl = base.with_rows(M)
-            case = Case(gnq, wl, dev, exact_inputs=True, l2_bytes=l2)
-            row = {"M": M}
-            for label, kernel, cluster in SWEEP_SHAPES:
-                gnq.set_launch_policy(kernel, cluster, 0, 0)
-                us, _ = time_case(case, dev)
-                row[label + "_us"] = round(us, 3)
-            gnq.set_launch_policy(0, 0, 0, 0)
-            row["auto_GB_s"] = round(wl.algorithmic_bytes() / (row["auto_us"] / 1e6) / 1e9, 1)
-            rows.append(row)
-            del case
-            torch.cuda.empty_cache()
+        for mode in modes:
+            for M in m_values:
+                wl = sweep_workload(mode, M)
+                case = Case(gnq, wl, dev, exact_inputs=(M * wl.H <= 2 ** 24), l2_bytes=l2)
+                row = {"mode": mode, "M": M, "H": wl.H}
+                shape = gnq.query_launch(M, wl.H, wl.mode, wl.dtype, residual=wl.residual,
+                                         write_y=wl.write_y)
+                row["auto_shape"] = kernel_name(*shape, wl)
+                for label, kernel, cluster in SWEEP_SHAPES:
+                    gnq.set_launch_policy(kernel, cluster, 0, 0)
+                    us, _ = time_case(case, dev)
+                    row[label + "_us"] = round(us, 3)
+                gnq.set_launch_policy(0, 0, 0, 0)
+                row["auto_GB_s"] = round(wl.algorithmic_bytes() / (row["auto_us"] / 1e6) / 1e9, 1)
+                rows.append(row)
+                del case
+                torch.cuda.empty_cache()
     finally:
         gnq.set_launch_policy(0, 0, 0, 0)
     return rows
@@ -697,8 +806,8 @@ def run_reference(args, rank: int):
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded normals)",
-        "config": {"workload": wl.name, "M": wl.M, "H": wl.H, "io_dtype": wl.dtype,
-                   "mode": wl.mode, "sample": sample_txt},
+        "config": workload_config(wl, int(os.environ.get("WORLD_SIZE", "1"))),
+        "sample": sample_txt,
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample_txt, "cpu_model": cpu_model()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -720,7 +829,7 @@ def main():
                     help="seconds of identical replays before and after the timed replay, "
                          "so the clock sampler sees the load")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--ref-budget", type=float, default=60.0)
+    ap.add_argument("--ref-budget", type=float, default=40.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-table", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

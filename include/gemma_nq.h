@@ -212,6 +212,34 @@ int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y,
 int gnq_set_pdl(int enable);
 
 /*
+ * Constant weights (off by default).  With enable = 1, later calls read the
+ * norm weight w and the quantization scale before they wait for the
+ * preceding kernel on their stream (programmatic dependent launch), so those
+ * reads overlap its tail.  The caller guarantees that no kernel that precedes
+ * a call on its stream, and may still be running, writes w or scale (true
+ * when they are model constants).  x, the partials and the residual are
+ * always read after the wait.  Results are identical either way.  enable = 0
+ * restores the default.  Not synchronised with calls in flight on other host
+ * threads.  Returns GNQ_ERR_SHAPE for other values.
+ */
+int gnq_set_constant_weights(int enable);
+
+/*
+ * Test hook for the failure path of the bounded waits (off by default).
+ * With enable = 1, later launches of the persistent streaming kernel in this
+ * process announce 16 bytes more per row than their copies deliver and give
+ * a wait at most ~2^20 clock cycles, so each CTA's wait for its first row
+ * gives up: the kernel sets bit 1 of the device error word, completes each
+ * outstanding barrier with one more valid 16-byte copy (from w into its own
+ * shared memory, so every copy has landed before it returns), and returns
+ * without writing any output.  Nothing outside the call's own buffers is
+ * touched; the row kernel is unaffected.  enable = 0 restores normal
+ * launches.  Not synchronised with calls in flight on other host threads.
+ * Returns GNQ_ERR_SHAPE for other values.
+ */
+int gnq_inject_wait_timeout(int enable);
+
+/*
  * Device error word of the current device.  Every wait inside a kernel is
  * bounded; a kernel whose wait gives up (about a second without progress)
  * skips the rest of its work, sets bit 1 here and returns, leaving its

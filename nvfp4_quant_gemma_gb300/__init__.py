@@ -11,12 +11,14 @@ from ._binding import (  # noqa: F401
     gemma_add_rms_norm,
     gemma_add_rms_norm_quant,
     gemma_add_rms_norm_quant_parts,
+    inject_wait_timeout,
     library_path,
     quantize_fp8_values,
     read_device_error,
     load,
     query_launch,
     set_launch_policy,
+    set_constant_weights,
     set_pdl,
     status_string,
 )

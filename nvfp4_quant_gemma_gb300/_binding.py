@@ -52,6 +52,8 @@ def load() -> ctypes.CDLL:
             "gnq_query_launch": [i64, i64, I, I, I, I, I, F, P, P, P, P],
             "gnq_read_device_error": [P, I],
             "gnq_set_pdl": [I],
+            "gnq_set_constant_weights": [I],
+            "gnq_inject_wait_timeout": [I],
             "gnq_quantize_fp8_values": [P, i64, P, P, P],
             "gnq_encode_e4m3_e2m1": [P, i64, P, P, P],
         }
@@ -69,7 +71,8 @@ def load() -> ctypes.CDLL:
 EXPORTS = ("gemma_add_rms_norm", "gemma_add_rms_norm_quant", "gemma_add_rms_norm_quant_parts",
            "add_rms_norm_quant", "gnq_status_string", "gnq_set_launch_policy",
            "gnq_read_device_error", "gnq_set_pdl", "gnq_encode_e4m3_e2m1",
-           "gnq_quantize_fp8_values", "gnq_query_launch")
+           "gnq_quantize_fp8_values", "gnq_query_launch", "gnq_set_constant_weights",
+           "gnq_inject_wait_timeout")
 
 
 def status_string(status: int) -> str:
@@ -268,6 +271,18 @@ def query_launch(M: int, H: int, mode, dtype: str = "bf16", k: int = 1, residual
 def set_pdl(enable: bool) -> None:
     """Programmatic dependent launch on (default) or off for later calls."""
     _check(load().gnq_set_pdl(1 if enable else 0), "gnq_set_pdl")
+
+
+def set_constant_weights(enable: bool) -> None:
+    """Read w and the scale before waiting on the preceding kernel (the caller
+    guarantees no preceding kernel writes them); off by default."""
+    _check(load().gnq_set_constant_weights(1 if enable else 0), "gnq_set_constant_weights")
+
+
+def inject_wait_timeout(enable: bool) -> None:
+    """Test hook: later streaming launches make their bounded waits give up
+    (device error bit 1, no outputs written); off by default."""
+    _check(load().gnq_inject_wait_timeout(1 if enable else 0), "gnq_inject_wait_timeout")
 
 
 def read_device_error(clear: bool = True) -> int:

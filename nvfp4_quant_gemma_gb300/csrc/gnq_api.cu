@@ -45,6 +45,11 @@ std::atomic<int> g_force_cluster{0};
 std::atomic<int> g_force_vpt{0};
 std::atomic<int> g_force_form{0};  // 0 auto, 1 fp32 form, 2 packed (lean) form
 std::atomic<int> g_pdl{1};  // 1: launch as programmatic dependents, 0: plain launches
+std::atomic<int> g_const_w{0};  // 1: w and scale are read before the wait on the preceding grid
+std::atomic<int> g_inject_timeout{0};  // test hook: streaming waits give up (see the header)
+
+constexpr long long kWaitLimit = 1LL << 31;      // cycles: about a second
+constexpr long long kTestWaitLimit = 1LL << 20;  // cycles: under a millisecond
 
 // Device properties and the error word's address, queried once per device
 // with that device current.
@@ -64,6 +69,36 @@ const DevInfo *dev_info() {
     }
     return &g_info[dev];
 }
+
+}  // namespace
+
+cudaError_t opt_in_dynamic_smem(const void *fn) {
+    struct Done {
+        int dev;
+        const void *fn;
+    };
+    static std::mutex mu;
+    static Done done[512];
+    static int n_done = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < n_done; ++i)
+        if (done[i].dev == dev && done[i].fn == fn) return cudaSuccess;
+    cudaFuncAttributes a;
+    int optin = 0;
+    if ((e = cudaFuncGetAttributes(&a, fn)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess)
+        return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             optin - (int)a.sharedSizeBytes);
+    if (e == cudaSuccess && n_done < 512) done[n_done++] = Done{dev, fn};
+    return e;
+}
+
+namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
@@ -321,6 +356,10 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
+    const bool inject = g_inject_timeout.load() != 0;
+    p.wait_limit = inject ? kTestWaitLimit : kWaitLimit;
+    p.tx_extra = inject ? 16u : 0u;
+    p.const_w = g_const_w.load();
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool parts = k > 1;
@@ -461,6 +500,18 @@ int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y,
 int gnq_set_pdl(int enable) {
     if (enable != 0 && enable != 1) return GNQ_ERR_SHAPE;
     gnq::g_pdl.store(enable);
+    return GNQ_OK;
+}
+
+int gnq_set_constant_weights(int enable) {
+    if (enable != 0 && enable != 1) return GNQ_ERR_SHAPE;
+    gnq::g_const_w.store(enable);
+    return GNQ_OK;
+}
+
+int gnq_inject_wait_timeout(int enable) {
+    if (enable != 0 && enable != 1) return GNQ_ERR_SHAPE;
+    gnq::g_inject_timeout.store(enable);
     return GNQ_OK;
 }
 

@@ -35,6 +35,9 @@ struct Params {
     int write_y;
     int stages;           // streaming kernel: rows in flight per CTA
     unsigned int *err;    // device error word
+    long long wait_limit; // clock cycles a bounded wait may spin
+    uint32_t tx_extra;    // test hook: bytes announced per row beyond the copies (0 or 16)
+    int const_w;          // w and scale are never written by a preceding kernel
 };
 
 // ---------------------------------------------------------------------------
@@ -549,12 +552,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: gives up after ~2^31 cycles (about a second) and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Bounded wait: gives up after `limit` cycles (2^31, about a second, unless
+// a test asks for less) and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > (1LL << 31)) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
 }

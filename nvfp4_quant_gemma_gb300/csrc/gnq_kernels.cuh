@@ -250,12 +250,27 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
         lc[v] = PRED && !ok[v] ? (int)rank * p.seg : col[v];
     }
 
+    // The weight and the quantizer constants: before the wait on the
+    // preceding grid when the caller guarantees no preceding kernel writes
+    // them (const_w), else after it with the other inputs.
+    uint4 rv[VPT][U], xv[VPT][U], wv[VPT][U];
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    auto load_w = [&]() {
+#pragma unroll
+        for (int v = 0; v < VPT; ++v)
+#pragma unroll
+            for (int c = 0; c < U; ++c) wv[v][c] = (PRED || ok[v]) ? ld_weight(p.w + lc[v] + 8 * c) : zero;
+    };
+    QuantCtx qc;
+    if (p.const_w) {
+        load_w();
+        qc = make_quant_ctx(p, MODE, es_smem, t, NT);
+    }
+
     pdl_wait();  // inputs may come from the preceding grid
     pdl_trigger();
 
     // ---- issue every load of the row segment up front ----
-    uint4 rv[VPT][U], xv[VPT][U], wv[VPT][U];
-    const uint4 zero = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int v = 0; v < VPT; ++v)
 #pragma unroll
@@ -304,12 +319,10 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
 #pragma unroll
             for (int c = 0; c < U; ++c) xv[v][c] = pack8<T>(&acc[v][8 * c]);
     }
-#pragma unroll
-    for (int v = 0; v < VPT; ++v)
-#pragma unroll
-        for (int c = 0; c < U; ++c) wv[v][c] = (PRED || ok[v]) ? ld_weight(p.w + lc[v] + 8 * c) : zero;
-
-    const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
+    if (!p.const_w) {
+        load_w();
+        qc = make_quant_ctx(p, MODE, es_smem, t, NT);
+    }
 
     // ---- h = dtype(a + residual), sum of squares ----
     uint4 hb[VPT][U];                        // packed h (the new residual)
@@ -481,7 +494,7 @@ template <int MODE, int VPT, bool LEAN> struct StreamForm {
 // FULL: the launch guarantees the row is exactly VPT units x threads.
 template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, float (*warp_ss)[32],
-                                            float *es_smem) {
+                                            float *es_smem, uint4 *topup) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     constexpr bool SW = StreamForm<MODE, VPT, LEAN>::smem_w;
     constexpr bool PRED = Pred<MODE>::value && !FULL;  // FULL: no unit is out of range
@@ -506,23 +519,28 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
         const int64_t m = blockIdx.x + (int64_t)i * G;
         const uint32_t bar = bars + 8u * s;
         const uint32_t dst = base + stage_bytes * s;
-        mbar_expect_tx(bar, stage_bytes);
+        mbar_expect_tx(bar, stage_bytes + p.tx_extra);
         for (int op = 0; op < p.k; ++op)
             bulk_g2s(dst + row_bytes * op, p.x + op * p.part_stride + m * p.H, row_bytes, bar);
         if (p.residual) bulk_g2s(dst + row_bytes * p.k, p.residual + m * p.H, row_bytes, bar);
     };
 
-    pdl_wait();  // inputs may come from the preceding grid
-    pdl_trigger();
-
-    if (t == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
-    }
-
-    // per-CTA constants: the weight (packed if LEAN, else bias + w in fp32),
-    // quantizer context
+    // wait for the preceding grid (its outputs may be this grid's inputs),
+    // then start the copies of the first rows
+    auto start_rows = [&]() {
+        pdl_wait();
+        pdl_trigger();
+        if (t == 0) {
+            for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
+        }
+    };
+    // The per-CTA constants below (the weight, packed if LEAN, else bias + w
+    // in fp32; the quantizer context) are read after that, or before it when
+    // the caller guarantees no preceding kernel writes w or the scale
+    // (const_w).
+    if (!p.const_w) start_rows();
     int col[VPT];
     bool ok[VPT];
     uint4 wq[VPT][LEAN ? U : 1];
@@ -547,7 +565,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                 Act<T>::unpack(w, f);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) f[i] = __fadd_rn(p.weight_bias, f[i]);
-                if constexpr (SW) {  // read back only by this thread (SW implies PRED)
+                if constexpr (SW) {  // read back only by this thread (lc: the loaded unit)
                     const int uu = lc[v] / E;
                     bw_s[(2 * c) * nunits + uu] = make_float4(f[0], f[1], f[2], f[3]);
                     bw_s[(2 * c + 1) * nunits + uu] = make_float4(f[4], f[5], f[6], f[7]);
@@ -561,6 +579,8 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
     const uint32_t b16 = p.weight_bias == 1.f ? one16<T>() : 0u;  // LEAN: bias 1 or 0
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
 
+    if (p.const_w) start_rows();
+
     __syncthreads();  // barriers initialised, table filled
 
     int s = 0;            // stage of row i (i mod S)
@@ -570,16 +590,23 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
         const int64_t row = m * (int64_t)p.H;
         const uint32_t stage = base + stage_bytes * s;
 
-        const bool arrived = mbar_wait_bounded(bars + 8u * s, parity);
+        const bool arrived = mbar_wait_bounded(bars + 8u * s, parity, p.wait_limit);
         if (__syncthreads_or(!arrived)) {
             // A copy never completed: record it, let the copies still in
             // flight land (bounded again) before the shared memory goes away.
+            // Under the test hook (tx_extra) the missing bytes are this
+            // kernel's own announcement: one more valid copy per outstanding
+            // row completes each barrier, so every copy has landed when the
+            // waits below return.
             if (t == 0) {
                 atomicOr(p.err, (unsigned)DEVERR_WAIT_TIMEOUT);
                 int sj = s;
                 uint32_t pj = parity;
                 for (int j = i; j < n_rows && j < i + S; ++j) {
-                    mbar_wait_bounded(bars + 8u * sj, pj);
+                    if (p.tx_extra)
+                        bulk_g2s((uint32_t)__cvta_generic_to_shared(&topup[sj]), p.w, p.tx_extra,
+                                 bars + 8u * sj);
+                    mbar_wait_bounded(bars + 8u * sj, pj, p.wait_limit);
                     if (++sj == S) {
                         sj = 0;
                         pj ^= 1u;
@@ -710,13 +737,14 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
 #define GNQ_STREAM_SMEM                                     \
     extern __shared__ __align__(128) uint8_t dsmem[];       \
     __shared__ __align__(16) float warp_ss[2][32];          \
-    __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
+    __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1]; \
+    __shared__ __align__(16) uint4 topup[4];
 
 // FP8, MXFP8 and no-quant streaming: the compiler's own register choice.
 template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem);
+    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem, topup);
 }
 
 // NVFP4 streaming: the StreamForm register budget.
@@ -725,7 +753,7 @@ __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) __maxnreg__((StreamForm
     stream_kernel_nvfp4(const __grid_constant__ Params p) {
     static_assert(MODE == MODE_NVFP4, "NVFP4 streaming only");
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem);
+    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem, topup);
 }
 #undef GNQ_STREAM_SMEM
 

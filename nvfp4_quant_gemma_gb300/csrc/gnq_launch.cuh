@@ -26,6 +26,14 @@ template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream);
 
+// Opts a kernel instance in to the largest dynamic shared memory one of its
+// CTAs may have on the current device (the device's opt-in limit less the
+// instance's static shared memory), once per device and instance.  The value
+// never changes, so calls from several host threads agree; each launch states
+// its own size in cudaLaunchConfig_t::dynamicSmemBytes.  (Defined in
+// gnq_api.cu.)
+cudaError_t opt_in_dynamic_smem(const void *fn);
+
 // Resident CTAs per SM of the streaming kernel instance for this shape (0 on
 // error); opts the instance in to `smem` bytes of dynamic shared memory.
 template <int MODE>
@@ -67,9 +75,7 @@ template <int MODE>
 int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
                          size_t smem) {
     void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, lean, true, full);
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-        return 0;
+    if (opt_in_dynamic_smem(reinterpret_cast<const void *>(fn)) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
         return 0;
@@ -81,9 +87,7 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
                         cudaStream_t stream) {
     void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.lean, ls.stream, ls.full);
     if (ls.stream) {
-        // opt in to the dynamic shared memory this launch needs (idempotent)
-        const cudaError_t e = cudaFuncSetAttribute(
-            fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ls.smem);
+        const cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void *>(fn));
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};

@@ -108,16 +108,41 @@ EXTRA_WORKLOADS = {
     ]
 }
 
-# The decode batch the headline throughput is quoted on.
-HEADLINE = "decode_m256_h4096_bf16_fp8_y"
+# The batch the headline throughput is quoted on: the largest configuration
+# (prefill, 16384 x 8192 fp16, static FP8 with an in-place residual; 939.5 MB
+# per call).
+HEADLINE = "prefill_m16384_h8192_fp16_fp8"
 
-# Batch sizes of the small-batch latency sweep (on the headline's H, dtype
-# and mode).
-SMALL_M = (1, 2, 4, 8, 16, 32, 64, 128, 256, 512, 1024)
+# The small-batch sweep: batch sizes M = 1 .. 8192 at H = 5120 (bf16, the
+# M = 2048 configuration's distributions), in both the static-FP8 and the
+# NVFP4 mode, as the launch-heuristic sweep of "vllm.models.qwen3_5.nvidia.
+# ops.fused_norm_quant" (gemma_add_rms_norm_quant) was taken.  129 and 192
+# are the batch sizes that sweep singles out.
+SMALL_M = (1, 2, 4, 8, 16, 32, 64, 96, 128, 129, 152, 192, 256, 384, 512, 1024, 2048, 4096, 8192)
+SWEEP_BASES = {
+    "nvfp4": "prefill_m2048_h5120_bf16_nvfp4_y",
+    "fp8": "sweep_h5120_bf16_fp8_y",
+}
+
+
+# Shapes used only as the base of the small-batch sweep (not bench lines).
+SWEEP_WORKLOADS = {
+    w.name: w for w in [
+        Workload("sweep_h5120_bf16_fp8_y", 2048, 5120, "bf16", "fp8", 0.05,
+                 write_y=True, residual=True, seed=2, r_var=9.0, n_outliers=8),
+    ]
+}
 
 
 def all_workloads() -> dict:
     return {**WORKLOADS, **EXTRA_WORKLOADS}
+
+
+def sweep_workload(mode: str, M: int) -> Workload:
+    """The small-batch sweep's workload of one mode at M rows."""
+    base = SWEEP_BASES[mode]
+    wl = WORKLOADS.get(base) or SWEEP_WORKLOADS[base]
+    return wl.with_rows(M)
 
 
 def outlier_channels(wl: Workload) -> torch.Tensor:

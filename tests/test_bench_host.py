@@ -50,11 +50,51 @@ def test_algorithmic_bytes(name):
     assert all_workloads()[name].algorithmic_bytes() == HAND_BYTES[name]
 
 
-def test_headline_bytes_and_rows():
+def test_headline_is_the_largest_configuration():
     wl = WORKLOADS[HEADLINE]
-    assert (wl.M, wl.H, wl.dtype, wl.mode, wl.write_y, wl.residual) == (256, 4096, "bf16", "fp8",
-                                                                         True, True)
-    assert wl.algorithmic_bytes() == 9445376
+    assert (wl.M, wl.H, wl.dtype, wl.mode, wl.write_y, wl.residual) == (16384, 8192, "fp16", "fp8",
+                                                                         False, True)
+    assert wl.algorithmic_bytes() == 939540480
+    assert wl.algorithmic_bytes() == max(w.algorithmic_bytes() for w in WORKLOADS.values())
+
+
+def test_both_arms_report_the_same_config():
+    """The GPU arm and the reference arm build `config` from the workload
+    alone, so the two lines of one workload carry identical configs."""
+    wl = WORKLOADS[HEADLINE]
+    a = bench.workload_config(wl, 1)
+    assert a == bench.workload_config(wl, 1)
+    assert a["workload"] == HEADLINE and a["l2"].startswith("inputs larger than L2")
+    assert bench.workload_config(wl, 2)["parallelism"] == "replicas2"
+    small = bench.workload_config(WORKLOADS["decode_m16_h2048_bf16_fp8"], 1)
+    assert "rotate" in small["l2"] and not small["l2"].startswith("inputs larger")
+
+
+def test_kernel_names_follow_the_launch_shape():
+    wl = WORKLOADS[HEADLINE]
+    assert bench.kernel_name(1, 1, 4, 1, wl) == \
+        "gnq::row_kernel<__half, MODE_FP8, parts=false, VPT=4, fp32>"
+    nv = WORKLOADS["prefill_m16384_h8192_fp16_nvfp4_nores"]
+    assert bench.kernel_name(2, 0, 4, 2, nv) == \
+        "gnq::stream_kernel_nvfp4<__half, MODE_NVFP4, parts=false, VPT=4, packed>"
+    assert bench.kernel_name(1, 4, 1, 1, wl).endswith("x 4-CTA cluster")
+
+
+def test_link_ceiling():
+    link = {"h2d_GB_s": 400.0, "d2h_GB_s": 200.0, "bidirectional_GB_s": 500.0}
+    # one way: max(4e8 / 400e9, 1e8 / 200e9) = 1 ms; both ways: 5e8 / 500e9 = 1 ms
+    assert abs(bench.link_ceiling(10 ** 9, 4 * 10 ** 8, 10 ** 8, link) - 1000.0) < 1e-6
+    link["bidirectional_GB_s"] = 250.0   # the two directions share the link: 2 ms
+    assert abs(bench.link_ceiling(10 ** 9, 4 * 10 ** 8, 10 ** 8, link) - 500.0) < 1e-6
+
+
+def test_small_batch_sweep_bases():
+    from nvfp4_quant_gemma_gb300.workloads import SMALL_M, sweep_workload
+    assert {1, 128, 129, 192, 8192} <= set(SMALL_M)
+    for mode in ("fp8", "nvfp4"):
+        wl = sweep_workload(mode, 129)
+        assert (wl.M, wl.H, wl.dtype, wl.mode, wl.residual, wl.write_y) == (129, 5120, "bf16",
+                                                                             mode, True, True)
 
 
 def _traffic_file(tmp_path, src_hash, rows):

@@ -1,32 +1,35 @@
 """Full-size parity: every workload (the five configurations and the MXFP8,
 plain-RMSNorm and norm-only variants) at its real size, launched exactly as
-bench.py launches it (automatic policy, same inputs recipe).
+bench.py launches it (automatic policy, same inputs recipe), compared with
+the oracle over the WHOLE tensor:
 
-* Sampled rows (first, last, a seeded random set) against the oracle: the
-  updated residual bit for bit, y within one ulp, codes and scales bit for
-  bit from the GPU's own y, scale padding untouched.
-* Whole-tensor properties from independent library arithmetic: the
-  residual equals torch's correctly rounded 16-bit add everywhere; FP8
-  codes equal torch's fp32 division + saturating cast of the GPU's y
-  everywhere; NVFP4 codes dequantize to within one code step of y; MXFP8
-  scales are the E8M0 exponents of the GPU's own block amax and its codes
-  torch's saturating cast of y over the exact power-of-two scale.
-* The configured write_y=False call gives the same codes as a write_y=True
-  call on the same inputs.
+* the updated residual bit for bit on every row;
+* y within one ulp of the oracle's fp64 norm on every row;
+* codes and scales bit for bit on every row when the oracle quantizes the
+  GPU's own y, and the NVFP4 scale padding untouched;
+* end to end (the oracle's own y -> codes) every differing code and scale
+  one step away, and at most 1e-4 of them differing.
+
+Independent library arithmetic pins the same tensors once more: the residual
+equals torch's correctly rounded 16-bit add everywhere; FP8 codes equal
+torch's fp32 division + saturating cast of the GPU's y; MXFP8 scales are the
+E8M0 exponents of the GPU's own block amax and its codes torch's saturating
+cast of y over the exact power-of-two scale.  The configured call (y not
+written, as bench times it) gives the same codes as a call that writes y in
+the same launch shape.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gnq_testutil import DTYPE_CODE, bits, u8, ulp_distance16, unpack_nibbles
+from gnq_testutil import DTYPE_CODE, bits, check_end_to_end, u8, ulp_distance16
 from nvfp4_quant_gemma_gb300.workloads import all_workloads, make_inputs
 
 pytestmark = pytest.mark.gpu
 
 OMODE = {"fp8": oracle.MODE_FP8, "nvfp4": oracle.MODE_NVFP4, "mxfp8": oracle.MODE_MXFP8,
          "none": oracle.MODE_NONE}
-N_SAMPLE = 24
 
 
 @pytest.fixture(scope="module")
@@ -125,69 +128,26 @@ def test_workload_full_size(gnq, name):
         ref_q = (yb32 * inv[..., None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
         assert torch.equal(q_b.view(torch.uint8), ref_q.view(torch.uint8).reshape(wl.M, wl.H))
         del yb32, amax, e, want, got, inv, ref_q
-    elif om == oracle.MODE_NVFP4:
-        # decode codes * sf / g and check |dequant - y| <= one code step
-        M, H = wl.M, wl.H
-        codes = torch.stack([q_b & 0xF, q_b >> 4], dim=-1).reshape(M, H).long()
-        table = torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6],
-                             device=dev)
-        vals = table[codes].reshape(M, H // 16, 16)
-        Kp = H // 16
-        m_idx = torch.arange(M, device=dev)[:, None]
-        b_idx = torch.arange(Kp, device=dev)[None, :]
-        off = ((m_idx // 128) * (Kp // 4) + b_idx // 4) * 512 + (m_idx % 32) * 16 \
-            + ((m_idx % 128) // 32) * 4 + b_idx % 4
-        sf = bs_b.view(torch.float8_e4m3fn).reshape(-1)[off.reshape(-1)].float().reshape(M, Kp)
-        g = float(wl.scale)
-        deq = vals * (sf / g)[..., None]
-        yv = y_b.float().reshape(M, H // 16, 16)
-        step = (sf / g)[..., None] * 2.0  # the largest E2M1 step is 2
-        unsat = ((sf > 0) & (sf < 448))[..., None]  # blocks whose scale neither saturated nor vanished
-        assert bool(((deq - yv).abs() <= step * 1.0001 + 1e-30)[unsat.expand_as(yv)].all())
-        del codes, vals, deq, yv, step
 
-    # sampled rows against the oracle
-    rng = np.random.default_rng(wl.seed)
-    rows = sorted({0, wl.M - 1, *rng.choice(wl.M, size=min(N_SAMPLE, wl.M), replace=False).tolist()})
-    xs = inp["x"][:, rows] if wl.k > 1 else inp["x"][rows]
-    rs = None if r0 is None else r0[rows]
-    ref = oracle.gemma_add_rms_norm_quant(bits(xs), None if rs is None else bits(rs),
-                                          bits(inp["weight"]), wl.eps, wl.scale, om, dc,
-                                          write_y=True, weight_bias=wl.weight_bias)
+    # every row against the oracle
+    r_in = None if r0 is None else bits(r0)
+    ref = oracle.gemma_add_rms_norm_quant(bits(inp["x"]), r_in, bits(inp["weight"]), wl.eps,
+                                          wl.scale, om, dc, write_y=True,
+                                          weight_bias=wl.weight_bias)
+    del r_in
     if r0 is not None:
-        assert np.array_equal(bits(r_a[rows]), ref["residual"])
-    gy = bits(y_b[rows])
+        assert np.array_equal(bits(r_a), ref["residual"])
+    gy = bits(y_b)
     assert int(ulp_distance16(gy, ref["y"]).max()) <= 1
     if om == oracle.MODE_NONE:
         assert torch.equal(y_a, y_b)
         return
     qo, bso = oracle.quantize_from_y(gy, wl.scale, om, dc)
-    assert np.array_equal(u8(q_a[rows]), qo)
-    if om == oracle.MODE_MXFP8:
-        assert np.array_equal(u8(bs_a[rows]), bso)
-    if om == oracle.MODE_NVFP4:
-        Kp = wl.H // 16
-        flat = u8(bs_a).reshape(-1)
-        for i, m in enumerate(rows):
-            got = flat[[oracle.swizzle_offset(m, b, Kp) for b in range(Kp)]]
-            want = bso.reshape(-1)[[oracle.swizzle_offset(i, b, Kp) for b in range(Kp)]]
-            assert np.array_equal(got, want)
-        # padding rows of the last 128-row tile stay untouched
-        Mp = oracle.round_up(wl.M, 128)
-        if Mp > wl.M:
-            pad = [oracle.swizzle_offset(m, b, Kp) for m in range(wl.M, Mp) for b in range(Kp)]
-            assert np.all(flat[pad] == 0xA5)
-    # end to end on the sampled rows
-    if om == oracle.MODE_NVFP4:
-        a = unpack_nibbles(u8(q_a[rows])).astype(np.int64)
-        b = unpack_nibbles(ref["q"]).astype(np.int64)
-        ra = np.where(a & 8, -(a & 7), a & 7)
-        rb = np.where(b & 8, -(b & 7), b & 7)
-    else:
-        a = u8(q_a[rows]).astype(np.int64)
-        b = ref["q"].astype(np.int64)
-        ra = np.where(a & 0x80, -(a & 0x7F), a & 0x7F)
-        rb = np.where(b & 0x80, -(b & 0x7F), b & 0x7F)
-    diff = np.abs(ra - rb)
-    assert int(diff.max(initial=0)) <= 1
-    assert np.count_nonzero(diff) <= max(1, int(1e-4 * diff.size))
+    gq = u8(q_a)
+    assert np.array_equal(gq, qo)
+    gbs = None if bs_a is None or om == oracle.MODE_FP8 else u8(bs_a)
+    if gbs is not None:
+        # NVFP4: the whole swizzled buffer, so the padding rows (filled with
+        # the oracle's sentinel before the call) must also be untouched
+        assert np.array_equal(gbs, bso)
+    check_end_to_end(gq, gbs, ref, om)

@@ -6,8 +6,13 @@ Rules (the method's correctness contract):
     2^-8 for bf16, 2^-11 for fp16) of the oracle's fp64 norm;
   * codes and block scales are bit-exact when the oracle quantizes the GPU's
     own y (the same fp32 decisions on both sides);
-  * end to end (oracle y -> oracle codes vs GPU codes) at most 1e-4 of the
-    elements differ, each by at most one adjacent code;
+  * end to end (oracle y -> oracle codes vs GPU codes) every differing code
+    is an adjacent code, and at most 1e-4 of the elements differ (checked
+    where a tensor holds at least 1e5 codes: below that the fraction is
+    under ten codes and the bound is not meaningful); the same rule for the
+    NVFP4 E4M3 block-scale bytes and the MXFP8 E8M0 scale codes (MXFP8 codes
+    are compared where the two scales agree: a scale one code apart
+    rescales its whole block by 2);
   * NVFP4 scale rows >= M, and bytes around every output, are untouched.
 """
 import numpy as np
@@ -15,8 +20,7 @@ import pytest
 import torch
 
 import oracle
-from gnq_testutil import (DTYPE_CODE, DTYPES, bits, e2m1_signed_rank, e4m3_signed_rank, u8,
-                          ulp_distance16, unpack_nibbles)
+from gnq_testutil import DTYPE_CODE, DTYPES, bits, check_end_to_end, u8, ulp_distance16
 
 pytestmark = pytest.mark.gpu
 
@@ -149,13 +153,7 @@ def run_case(gnq, x, r, w, mode, scale, write_y, dtype, eps=1e-6, weight_bias=1.
         assert np.array_equal(u8(full["bs"]), bso)
     # end to end: oracle codes vs GPU codes
     if check_e2e:
-        if om == oracle.MODE_NVFP4:
-            a, b = e2m1_signed_rank(unpack_nibbles(gq)), e2m1_signed_rank(unpack_nibbles(ref["q"]))
-        else:
-            a, b = e4m3_signed_rank(gq), e4m3_signed_rank(ref["q"])
-        diff = np.abs(a - b)
-        assert int(diff.max(initial=0)) <= 1
-        assert np.count_nonzero(diff) <= max(1, int(1e-4 * diff.size))
+        check_end_to_end(gq, None if full["bs"] is None else u8(full["bs"]), ref, om)
 
 
 # --- hardware encoders vs the oracle's reading ----------------------------------
@@ -192,7 +190,7 @@ SMALL_M = [1, 3, 127, 129, 300]
 @pytest.mark.parametrize("H", [64, 2048, 5120])
 def test_small_shapes(gnq, dtype, mode, scale, M, H):
     x, r, w = _make(M, H, dtype, seed=M * 7 + H)
-    run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 1), dtype=dtype, check_e2e=(M * H >= 1e5))
+    run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 1), dtype=dtype)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
@@ -273,8 +271,7 @@ def test_streaming_kernel(gnq, dtype, mode, scale, M, H, k, res, form):
     register forms."""
     x, r, w = _make(M, H, dtype, seed=M + H + k, k=k, residual=res)
     with forced_policy(gnq, 2, 0, 0, form):
-        run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 0), dtype=dtype,
-                 check_e2e=(M * H >= 1e5))
+        run_case(gnq, x, r, w, mode, scale, write_y=(M % 2 == 0), dtype=dtype)
     assert gnq.read_device_error() == 0
 
 
@@ -595,3 +592,69 @@ def test_binding_rejects_bad_buffers(gnq):
     with pytest.raises(ValueError):
         gnq.gemma_add_rms_norm_quant_parts(torch.stack([x, x]), r, w, 1e-6, s, "fp8",
                                            out=(q, None, None))              # q sized for NVFP4
+
+
+def test_bounded_wait_gives_up_and_the_next_call_is_clean(gnq):
+    """The failure path of the streaming kernel's bounded waits, on the GPU
+    without a fault: under the library's test hook every row announces 16
+    bytes more than its copies deliver, so no barrier can complete and each
+    CTA's first wait runs out (after ~2^20 cycles).  The kernel must set the
+    timeout bit of the device error word, complete its barriers itself with
+    one more valid copy, and return without writing any output; the next
+    normal call must then pass the whole parity contract."""
+    dev = torch.device("cuda")
+    M, H = 700, 2048
+    x, _, w = _make(M, H, "bf16", seed=61, residual=False)
+    xd, wd = x.to(dev), w.to(dev)
+    sd = torch.tensor([0.05], device=dev)
+    assert gnq.read_device_error(clear=True) == 0
+    q, _, _ = gnq.alloc_outputs(M, H, "fp8", False, xd)
+    q.view(torch.uint8).fill_(0xA5)
+    with forced_policy(gnq, 2):
+        gnq.inject_wait_timeout(True)
+        try:
+            gnq.gemma_add_rms_norm_quant(xd, None, wd, 1e-6, sd, "fp8", write_y=False,
+                                         out=(q, None, None))
+            torch.cuda.synchronize()
+        finally:
+            gnq.inject_wait_timeout(False)
+        assert gnq.read_device_error(clear=True) & 1, "the timeout bit was not set"
+        assert bool((q.view(torch.uint8) == 0xA5).all()), "a timed-out call wrote codes"
+        run_case(gnq, x, None, w, "fp8", 0.05, write_y=False, dtype="bf16")
+    assert gnq.read_device_error() == 0
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0), ("mxfp8", 0.0)])
+def test_constant_weights_flag(gnq, kernel, mode, scale):
+    """With the constant-weights flag the kernels read w and the scale before
+    they wait on the preceding kernel: single calls keep the parity contract,
+    and a dependent chain (each call consuming the residual the previous one
+    wrote) gives the bits of the default launches."""
+    dev = torch.device("cuda")
+    x, r, w = _make(300, 4096, "bf16", seed=67)
+    gnq.set_constant_weights(True)
+    try:
+        with forced_policy(gnq, kernel):
+            run_case(gnq, x, r, w, mode, scale, write_y=True, dtype="bf16")
+    finally:
+        gnq.set_constant_weights(False)
+    xd, wd = x.to(dev), w.to(dev)
+    sd = torch.tensor([scale], device=dev)
+
+    def chain(const_w):
+        gnq.set_constant_weights(const_w)
+        try:
+            rd = r.to(dev)
+            outs = [gnq.alloc_outputs(300, 4096, mode, True, xd) for _ in range(4)]
+            with forced_policy(gnq, kernel):
+                for o in outs:
+                    gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
+            torch.cuda.synchronize()
+            return [rd.clone()] + [t.view(torch.uint8).clone() for o in outs for t in o
+                                   if t is not None]
+        finally:
+            gnq.set_constant_weights(False)
+
+    assert all(torch.equal(a, b) for a, b in zip(chain(False), chain(True)))
+    assert gnq.read_device_error() == 0
