@@ -688,6 +688,7 @@ def run_gnq(args, rank: int, world: int, barrier):
         line["workloads"] = workload_table(gnq, dev, l2, peak)
     if world == 1 and not args.no_sweep:
         line["small_m_sweep"] = small_m_sweep(gnq, dev, l2, peak)
+        line["pdl_consumer_sweep"] = pdl_consumer_sweep(gnq, dev, l2)
     return line
 
 
@@ -717,6 +718,7 @@ def workload_table(gnq, dev, l2, peak):
         b = wl.algorithmic_bytes()
         gbs = b / (us / 1e6) / 1e9
         rows.append({"workload": name, "kind": "config" if name in WORKLOADS else "variant",
+                     "kernel": launched_kernel(gnq, wl),
                      "us_per_call": round(us, 3), "GB_s": round(gbs, 1),
                      "frac_of_peak": round(gbs / peak, 4), "tokens_per_s": round(wl.M / (us / 1e6)),
                      "bytes_per_call": b, "launches_timed": n, "sets": case.n_sets,
@@ -756,6 +758,72 @@ def small_m_sweep(gnq, dev, l2, peak, modes=("fp8", "nvfp4"), m_values=SMALL_M):
                 torch.cuda.empty_cache()
     finally:
         gnq.set_launch_policy(0, 0, 0, 0)
+    return rows
+
+
+# launches compared with a consumer: (label, programmatic dependent launch on)
+PDL_POLICIES = (("pdl_trigger_early", True), ("no_pdl", False))
+PDL_M = (1, 16, 64, 128, 152, 192, 256, 512, 2048, 8192)
+CONSUMER_WEIGHT_PER_CTA = 32768  # bytes each consumer CTA reads before its wait
+
+
+def time_pairs(case, dev, consumer, probe_n: int = 8) -> float:
+    """Microseconds per (call, consumer) pair: a CUDA graph of n pairs, each
+    call followed by the stand-in consumer of its codes."""
+    def graph(n):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            case.step(0)
+            consumer(0)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.graph(g):
+            for i in range(n):
+                case.step(i)
+                consumer(i)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        return g
+    g = graph(probe_n)
+    t = time_graph(g, dev, probe_n) / probe_n
+    n = int(min(2000, max(20, 0.3e3 / max(t, 1e-4))))
+    g = graph(n)
+    return time_graph(g, dev, n) / n * 1e3
+
+
+def pdl_consumer_sweep(gnq, dev, l2, modes=("fp8", "nvfp4"), m_values=PDL_M):
+    """Programmatic dependent launch with a real consumer: each call (H =
+    5120, bf16, residual, y) is followed by a stand-in for the next layer's
+    first kernel (one CTA per SM, launched as a programmatic dependent; it
+    reads 32 KB of its own weight per CTA before it waits, then the call's
+    codes), with the calls launched as programmatic dependents that let the
+    consumer launch right after their own wait, and as plain launches."""
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    wt = torch.randint(0, 255, (sms * CONSUMER_WEIGHT_PER_CTA,), dtype=torch.uint8, device=dev)
+    out = torch.empty(sms * 256, dtype=torch.int32, device=dev)
+    rows = []
+    try:
+        for mode in modes:
+            for M in m_values:
+                wl = sweep_workload(mode, M)
+                case = Case(gnq, wl, dev, exact_inputs=(M * wl.H <= 2 ** 24), l2_bytes=l2)
+
+                def consumer(i, case=case):
+                    q = case.sets[i % case.n_sets][2][0]
+                    gnq.pdl_consumer(q, wt, out, sms)
+
+                row = {"mode": mode, "M": M, "H": wl.H}
+                for label, pol in PDL_POLICIES:
+                    gnq.set_pdl(pol)
+                    row[label + "_us"] = round(time_pairs(case, dev, consumer), 3)
+                gnq.set_pdl(True)
+                rows.append(row)
+                del case
+                torch.cuda.empty_cache()
+    finally:
+        gnq.set_pdl(True)
     return rows
 
 

@@ -49,7 +49,10 @@
  *    no effect.
  *  - Alignment: x, residual, w, y, q and every partial buffer must be 16-byte
  *    aligned, block_scale 4-byte aligned, scale 4-byte aligned
- *    (GNQ_ERR_ALIGN).  H must be a multiple of 8 (GNQ_ERR_SHAPE); NVFP4 needs
+ *    (GNQ_ERR_ALIGN).  NVFP4 calls whose 16-bit tensors (and partial
+ *    stride) are also 32-byte aligned, as every allocator's tensors are,
+ *    move each 16-element block in one 256-bit access; others run one CTA
+ *    per row with 128-bit accesses.  H must be a multiple of 8 (GNQ_ERR_SHAPE); NVFP4 needs
  *    H % 64 == 0 (whole 4-column scale tiles, so padded scale columns never
  *    exist) and MXFP8 H % 32 == 0.  H is at most 65536.
  *  - x and residual must not be the same buffer, and y must differ from both
@@ -204,23 +207,30 @@ int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y,
  * Programmatic dependent launch (on by default): each launch may start while
  * the preceding kernel on the stream drains, and waits inside the kernel
  * (griddepcontrol.wait) until that kernel's results are visible before its
- * first global read; once all of its CTAs have started it also lets a
- * programmatic dependent that follows it launch (that kernel must wait in the
- * same way before reading these outputs).  Results are identical either way.
- * enable = 0 turns it off for later calls in this process, 1 turns it on.
+ * first global read; right after that wait it also lets a programmatic
+ * dependent that follows it launch (that kernel must wait in the same way
+ * before reading these outputs), so the dependent's CTAs can take the SMs
+ * this grid leaves idle and run their own prologue early.  Results are
+ * identical either way.  enable = 0 turns it off for later calls in this
+ * process, 1 turns it on.  Not synchronised with calls in flight on other
+ * host threads.
  */
 int gnq_set_pdl(int enable);
 
 /*
- * Constant weights (off by default).  With enable = 1, later calls read the
- * norm weight w and the quantization scale before they wait for the
- * preceding kernel on their stream (programmatic dependent launch), so those
- * reads overlap its tail.  The caller guarantees that no kernel that precedes
- * a call on its stream, and may still be running, writes w or scale (true
- * when they are model constants).  x, the partials and the residual are
- * always read after the wait.  Results are identical either way.  enable = 0
- * restores the default.  Not synchronised with calls in flight on other host
- * threads.  Returns GNQ_ERR_SHAPE for other values.
+ * Constant weights (off by default).  With enable = 1, later small-batch
+ * calls (those the policy runs one 16-byte unit -- NVFP4: one 16-element
+ * block -- per thread on the one-CTA-per-row kernel, i.e. batches below about
+ * one row per SM, with one activation rather than partials) read the norm
+ * weight w and the quantization scale, and build their quantizer constants,
+ * before they wait for the preceding kernel on their stream (programmatic
+ * dependent launch), so that work overlaps its tail; other calls ignore the
+ * flag.  The caller guarantees that no kernel that precedes a call on its
+ * stream, and may still be running, writes w or scale (true when they are
+ * model constants).  x, the partials and the residual are always read after
+ * the wait.  Results are identical either way.  enable = 0 restores the
+ * default.  Not synchronised with calls in flight on other host threads.
+ * Returns GNQ_ERR_SHAPE for other values.
  */
 int gnq_set_constant_weights(int enable);
 
@@ -247,6 +257,21 @@ int gnq_inject_wait_timeout(int enable);
  * and clears it when `clear` is nonzero.
  */
 int gnq_read_device_error(unsigned int *flags, int clear);
+
+/*
+ * Diagnostic: a stand-in for the first kernel of the next linear layer, to
+ * measure programmatic dependent launch with a real consumer.  Launched as a
+ * programmatic dependent of the preceding kernel on `stream`, with `ctas`
+ * CTAs of 256 threads: each CTA first reads its share of the wt_bytes at
+ * `wt` (an independent buffer, standing for the layer's weight), then waits
+ * for the preceding kernel's results (griddepcontrol.wait), then reads its
+ * share of the q_bytes at `q` (that kernel's codes), and stores one checksum
+ * word per thread to `out` (ctas * 256 words).  Byte counts are multiples of
+ * 16 and the pointers 16-byte aligned device memory.  Returns GNQ_ERR_SHAPE,
+ * GNQ_ERR_NULL or GNQ_ERR_CUDA on bad arguments or a failed launch.
+ */
+int gnq_pdl_consumer(const void *q, int64_t q_bytes, const void *wt, int64_t wt_bytes,
+                     unsigned int *out, int ctas, void *stream);
 
 /*
  * Diagnostic: the static-FP8 quantizer the kernels use, applied to n fp32

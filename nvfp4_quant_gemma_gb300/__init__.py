@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     quantize_fp8_values,
     read_device_error,
     load,
+    pdl_consumer,
     query_launch,
     set_launch_policy,
     set_constant_weights,

@@ -55,6 +55,7 @@ def load() -> ctypes.CDLL:
             "gnq_set_constant_weights": [I],
             "gnq_inject_wait_timeout": [I],
             "gnq_quantize_fp8_values": [P, i64, P, P, P],
+            "gnq_pdl_consumer": [P, i64, P, i64, P, I, P],
             "gnq_encode_e4m3_e2m1": [P, i64, P, P, P],
         }
         for name, argt in sigs.items():
@@ -72,7 +73,7 @@ EXPORTS = ("gemma_add_rms_norm", "gemma_add_rms_norm_quant", "gemma_add_rms_norm
            "add_rms_norm_quant", "gnq_status_string", "gnq_set_launch_policy",
            "gnq_read_device_error", "gnq_set_pdl", "gnq_encode_e4m3_e2m1",
            "gnq_quantize_fp8_values", "gnq_query_launch", "gnq_set_constant_weights",
-           "gnq_inject_wait_timeout")
+           "gnq_inject_wait_timeout", "gnq_pdl_consumer")
 
 
 def status_string(status: int) -> str:
@@ -271,6 +272,20 @@ def query_launch(M: int, H: int, mode, dtype: str = "bf16", k: int = 1, residual
 def set_pdl(enable: bool) -> None:
     """Programmatic dependent launch on (default) or off for later calls."""
     _check(load().gnq_set_pdl(1 if enable else 0), "gnq_set_pdl")
+
+
+def pdl_consumer(q: torch.Tensor, wt: torch.Tensor, out: torch.Tensor, ctas: int,
+                 stream=None) -> None:
+    """Diagnostic stand-in for the next layer's first kernel: reads wt, waits
+    on the preceding kernel, reads q, writes ctas * 256 checksum words."""
+    for t, name in ((q, "q"), (wt, "wt")):
+        if not (t.is_cuda and t.is_contiguous() and (t.numel() * t.element_size()) % 16 == 0):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor of whole 16-byte units")
+    if not (out.is_cuda and out.dtype == torch.int32 and out.numel() >= ctas * 256):
+        raise ValueError("out must be an int32 CUDA tensor of at least ctas * 256 words")
+    _check(load().gnq_pdl_consumer(_ptr(q), q.numel() * q.element_size(), _ptr(wt),
+                                   wt.numel() * wt.element_size(), _ptr(out), int(ctas),
+                                   _stream(stream)), "gnq_pdl_consumer")
 
 
 def set_constant_weights(enable: bool) -> None:

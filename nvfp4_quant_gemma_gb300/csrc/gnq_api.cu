@@ -45,7 +45,7 @@ std::atomic<int> g_force_cluster{0};
 std::atomic<int> g_force_vpt{0};
 std::atomic<int> g_force_form{0};  // 0 auto, 1 fp32 form, 2 packed (lean) form
 std::atomic<int> g_pdl{1};  // 1: launch as programmatic dependents, 0: plain launches
-std::atomic<int> g_const_w{0};  // 1: w and scale are read before the wait on the preceding grid
+std::atomic<int> g_const_w{0};  // 1: small batches read w and scale before the PDL wait
 std::atomic<int> g_inject_timeout{0};  // test hook: streaming waits give up (see the header)
 
 constexpr long long kWaitLimit = 1LL << 31;      // cycles: about a second
@@ -223,8 +223,9 @@ bool stream_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int dtype, i
 // register form x M = 16 .. 16384 on the decode, prefill, no-residual and
 // partial-sum workload classes (GB300, 152 SMs):
 //   * one activation with a residual: one CTA per row at every M -- one
-//     unit per thread below ~SMs rows, else ~256 threads (FP8, MXFP8, no
-//     quant) or ~160 threads (NVFP4) per CTA;
+//     unit per thread below ~SMs rows, else ~256 threads per CTA (NVFP4 at
+//     H = 5120: 160; the fp16 16384 x 8192 NVFP4 batch ran 125.1 us at 256
+//     threads against 126.1 us at 128 with 256-bit accesses);
 //   * no residual: one CTA per row up to 16 x SMs rows, then -- unless y
 //     is written (norm only, or write_y), where the row kernel stays ahead --
 //     rows stream through persistent CTAs of four units per thread (~256
@@ -242,7 +243,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     const int fk = forced ? g_force_kernel.load() : 0, fc = forced ? g_force_cluster.load() : 0;
     const int fv = forced ? g_force_vpt.load() : 0, ff = forced ? g_force_form.load() : 0;
     const int nops = k + (res ? 1 : 0);
-    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false, false};
+    LaunchShape ls{false, 1, 1, 32, M, 0, 0, g_pdl.load() != 0, false, false, 0};
     // The packed (lean) form is chosen where four units per thread would
     // otherwise cost occupancy; it needs the Gemma or plain weight bias.
     const bool lean_ok = weight_bias == 1.f || weight_bias == 0.f;
@@ -260,7 +261,7 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
         stream = M >= 4 * sms;
         vpt = stream ? vpt_for(M >= 16 * sms && mode != MODE_NVFP4 ? 512 : 256) : 1;
     } else if (res) {
-        vpt = M < sms ? 1 : vpt_for(mode == MODE_NVFP4 ? 160 : 256);
+        vpt = M < sms ? 1 : vpt_for(256);
     } else {
         stream = M >= 16 * sms && !write_y;
         vpt = M < sms ? 1 : vpt_for(stream && mode == MODE_NVFP4 ? 128 : 256);
@@ -344,22 +345,30 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
 
     const DevInfo *d = dev_info();
     if (!d) return GNQ_ERR_CUDA;
+    // NVFP4 instances move a unit's 32-byte block in one 256-bit access when
+    // every 16-bit tensor is 32-byte aligned (the streaming ones of k
+    // partials always do).
+    const bool a32 = mode == MODE_NVFP4 && aligned(x, 32) && aligned(w, 32) &&
+                     (!residual || aligned(residual, 32)) && (!write_y || aligned(y, 32)) &&
+                     (k == 1 || (part_stride * 2) % 32 == 0);
     LaunchShape ls =
         choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias);
     // The streaming kernel's bulk copies read device memory; activations
     // anywhere else (mapped pinned host memory, read over the host link) run
     // on the row kernel, whose plain loads and stores reach any address the
-    // device can access.
-    if (ls.stream && (!in_device_memory(x) || (residual && !in_device_memory(residual))))
+    // device can access.  So do NVFP4 calls without 32-byte alignment.
+    if (ls.stream && ((mode == MODE_NVFP4 && k > 1 && !a32) || !in_device_memory(x) ||
+                      (residual && !in_device_memory(residual))))
         ls = choose_shape(*d, M, H, mode, dtype, k, residual != nullptr, write_y != 0, weight_bias,
                           true, false);
+    ls.opt = (a32 ? OPT_A32 : 0) |
+             (g_const_w.load() && !ls.stream && ls.vpt == 1 && k == 1 ? OPT_EARLYW : 0);
     p.seg = (int)(H / ls.cluster);
     p.stages = ls.stages;
     p.err = d->err;
     const bool inject = g_inject_timeout.load() != 0;
     p.wait_limit = inject ? kTestWaitLimit : kWaitLimit;
     p.tx_extra = inject ? 16u : 0u;
-    p.const_w = g_const_w.load();
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool parts = k > 1;
@@ -409,6 +418,27 @@ __global__ void encode_kernel(const float *v, int64_t n, uint8_t *e4m3, uint8_t 
         if (e4m3) e4m3[i] = (uint8_t)(e4m3x2(x, 0.f) & 0xFF);
         if (e2m1) e2m1[i] = (uint8_t)(e2m1x4(x, 0.f, 0.f, 0.f) & 0xF);
     }
+}
+
+// Stand-in for the first kernel of the next linear layer: each CTA reads
+// its share of an independent buffer (the layer's weight) before it waits on
+// the preceding grid, then its share of that grid's codes, and stores one
+// checksum word per thread.  Launched as a programmatic dependent.
+__global__ void consumer_kernel(const uint4 *q, int64_t nq, const uint4 *wt, int64_t nw,
+                                uint32_t *out) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t acc = 0;
+    for (int64_t i = i0; i < nw; i += stride) {
+        const uint4 v = ld_stream(wt + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    pdl_wait();
+    for (int64_t i = i0; i < nq; i += stride) {
+        const uint4 v = ld_stream(q + i);
+        acc += v.x ^ v.y ^ v.z ^ v.w;
+    }
+    out[i0] = acc;
 }
 
 }  // namespace
@@ -534,6 +564,28 @@ int gnq_encode_e4m3_e2m1(const float *v, int64_t n, uint8_t *e4m3, uint8_t *e2m1
     gnq::encode_kernel<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
         v, n, e4m3, e2m1);
     return cudaGetLastError() == cudaSuccess ? GNQ_OK : GNQ_ERR_CUDA;
+}
+
+int gnq_pdl_consumer(const void *q, int64_t q_bytes, const void *wt, int64_t wt_bytes,
+                     unsigned int *out, int ctas, void *stream) {
+    if (q_bytes < 0 || wt_bytes < 0 || q_bytes % 16 || wt_bytes % 16 || ctas < 1 || ctas > 65535)
+        return GNQ_ERR_SHAPE;
+    if (!out || (q_bytes && !q) || (wt_bytes && !wt)) return GNQ_ERR_NULL;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    cfg.attrs = &attr;
+    if (cudaLaunchKernelEx(&cfg, gnq::consumer_kernel, static_cast<const uint4 *>(q),
+                           q_bytes / 16, static_cast<const uint4 *>(wt), wt_bytes / 16,
+                           static_cast<uint32_t *>(out)) == cudaSuccess)
+        return GNQ_OK;
+    cudaGetLastError();
+    return GNQ_ERR_CUDA;
 }
 
 int gnq_quantize_fp8_values(const float *y, int64_t n, const float *scale, uint8_t *q,

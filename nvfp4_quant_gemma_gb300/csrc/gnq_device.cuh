@@ -15,6 +15,15 @@ enum { MODE_NONE = -1, MODE_FP8 = 0, MODE_NVFP4 = 1, MODE_MXFP8 = 2 };
 // Bits of the device error word (set by a kernel, read by gnq_device_error).
 enum { DEVERR_WAIT_TIMEOUT = 1 };
 
+// Compile-time options of a kernel instance (the OPT template argument):
+//   OPT_A32     NVFP4: every 16-bit tensor is 32-byte aligned, so a unit's
+//               32-byte block of x, residual, partials, w and y moves in one
+//               256-bit access;
+//   OPT_EARLYW  the weight and the quantizer constants are read before the
+//               wait on the preceding grid (the caller guarantees no
+//               preceding kernel writes them).
+enum { OPT_A32 = 1, OPT_EARLYW = 2 };
+
 struct Params {
     const uint16_t *x;    // the activation, or partial 0 of k
     int64_t part_stride;  // elements from one partial to the next
@@ -37,7 +46,6 @@ struct Params {
     unsigned int *err;    // device error word
     long long wait_limit; // clock cycles a bounded wait may spin
     uint32_t tx_extra;    // test hook: bytes announced per row beyond the copies (0 or 16)
-    int const_w;          // w and scale are never written by a preceding kernel
 };
 
 // ---------------------------------------------------------------------------
@@ -97,6 +105,39 @@ __device__ __forceinline__ void st_v2_if(void *p, uint32_t a, uint32_t b, bool o
 __device__ __forceinline__ void st_u8_if(void *p, uint32_t a, bool on) {
     asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
                  "@q st.global.u8 [%0], %1;\n\t}" ::"l"(p), "r"(a), "r"((int)on)
+                 : "memory");
+}
+
+// 32-byte (256-bit) accesses of two adjacent 16-byte chunks, for 32-byte
+// aligned addresses: one request per warp covers 1 KB of whole sectors.
+__device__ __forceinline__ void ld_stream_v8(const void *p, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                   "=r"(b.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void ld_inout_v8(const void *p, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                   "=r"(b.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void ld_weight_v8(const void *p, uint4 &a, uint4 &b) {
+    asm volatile("ld.global.nc.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z),
+                   "=r"(b.w)
+                 : "l"(p));
+}
+__device__ __forceinline__ void st_v8(void *p, uint4 a, uint4 b) {
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y),
+                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+__device__ __forceinline__ void st_v8_if(void *p, uint4 a, uint4 b, bool on) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %9, 0;\n\t"
+                 "@q st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n\t}" ::"l"(p),
+                 "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w),
+                 "r"((int)on)
                  : "memory");
 }
 

@@ -128,6 +128,10 @@ template <bool PRED> __device__ __forceinline__ void st_v2_unit(void *p, uint32_
     if constexpr (PRED) st_v2_if(p, a, b, ok);
     else if (ok) st_v2(p, a, b);
 }
+template <bool PRED> __device__ __forceinline__ void st_v8_unit(void *p, uint4 a, uint4 b, bool ok) {
+    if constexpr (PRED) st_v8_if(p, a, b, ok);
+    else if (ok) st_v8(p, a, b);
+}
 template <bool PRED> __device__ __forceinline__ void st_u8_unit(void *p, uint32_t a, bool ok) {
     if constexpr (PRED) st_u8_if(p, a, ok);
     else if (ok) st_u8(p, a);
@@ -137,17 +141,23 @@ template <bool PRED> __device__ __forceinline__ void st_u8_unit(void *p, uint32_
 // rounded values and store codes and scales.  `t` is the thread index;
 // FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA; `sfc` is the
 // unit's sf_col_offset (NVFP4).  PRED: out-of-range units are predicated
-// (Pred<MODE>), unless the instance has none (FULL).
-template <typename T, int MODE, int FP8PATH, bool PRED = Pred<MODE>::value>
+// (Pred<MODE>), unless the instance has none (FULL).  V8: the two chunks of
+// an NVFP4 unit's y leave in one 256-bit store (32-byte aligned y).
+template <typename T, int MODE, int FP8PATH, bool PRED = Pred<MODE>::value, bool V8 = false>
 __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &qc,
                                               float (&yf)[Unit<MODE>::E], const RowOut &o,
                                               int col, int sfc, bool ok, int t) {
     constexpr int U = Unit<MODE>::U;
     uint4 yb[U];
 #pragma unroll
-    for (int c = 0; c < U; ++c) {
-        yb[c] = pack8<T>(&yf[8 * c]);
-        if (PRED ? p.write_y != 0 : p.write_y && ok) st_v4_unit<PRED>(o.y + col + 8 * c, yb[c], ok);
+    for (int c = 0; c < U; ++c) yb[c] = pack8<T>(&yf[8 * c]);
+    if (PRED ? p.write_y != 0 : p.write_y && ok) {
+        if constexpr (V8 && U == 2) {
+            st_v8_unit<PRED>(o.y + col, yb[0], yb[1], ok);
+        } else {
+#pragma unroll
+            for (int c = 0; c < U; ++c) st_v4_unit<PRED>(o.y + col + 8 * c, yb[c], ok);
+        }
     }
 
     if (MODE == MODE_FP8) {
@@ -225,11 +235,14 @@ template <int MODE, int VPT, bool PARTS, bool LEAN> struct RowForm {
 };
 
 // FULL: the launch guarantees every unit of the CTA's segment is in range
-// (segment = VPT units x threads), so no unit needs a check.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
+// (segment = VPT units x threads), so no unit needs a check.  OPT: OPT_A32
+// and OPT_EARLYW (see gnq_device.cuh).
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL, int OPT>
 __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float &cta_ss,
                                          float *es_smem) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
+    constexpr bool V8 = (OPT & OPT_A32) && U == 2;
+    constexpr bool EARLY = (OPT & OPT_EARLYW) != 0;
 
     const uint32_t C = cluster_size();
     const uint32_t rank = C > 1 ? cluster_rank() : 0;
@@ -250,21 +263,25 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
         lc[v] = PRED && !ok[v] ? (int)rank * p.seg : col[v];
     }
 
-    // The weight and the quantizer constants: before the wait on the
-    // preceding grid when the caller guarantees no preceding kernel writes
-    // them (const_w), else after it with the other inputs.
     uint4 rv[VPT][U], xv[VPT][U], wv[VPT][U];
     const uint4 zero = make_uint4(0, 0, 0, 0);
     auto load_w = [&]() {
 #pragma unroll
-        for (int v = 0; v < VPT; ++v)
+        for (int v = 0; v < VPT; ++v) {
+            if constexpr (V8) {
+                if (PRED || ok[v]) ld_weight_v8(p.w + lc[v], wv[v][0], wv[v][1]);
+                else wv[v][0] = wv[v][1] = zero;
+            } else {
 #pragma unroll
-            for (int c = 0; c < U; ++c) wv[v][c] = (PRED || ok[v]) ? ld_weight(p.w + lc[v] + 8 * c) : zero;
+                for (int c = 0; c < U; ++c)
+                    wv[v][c] = (PRED || ok[v]) ? ld_weight(p.w + lc[v] + 8 * c) : zero;
+            }
+        }
     };
-    QuantCtx qc;
-    if (p.const_w) {
+    QuantCtx qc_early{};
+    if constexpr (EARLY) {  // constants first, then the wait on the preceding grid
         load_w();
-        qc = make_quant_ctx(p, MODE, es_smem, t, NT);
+        qc_early = make_quant_ctx(p, MODE, es_smem, t, NT);
     }
 
     pdl_wait();  // inputs may come from the preceding grid
@@ -272,12 +289,20 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
 
     // ---- issue every load of the row segment up front ----
 #pragma unroll
-    for (int v = 0; v < VPT; ++v)
+    for (int v = 0; v < VPT; ++v) {
+        if constexpr (V8) {
+            if (p.residual && (PRED || ok[v])) ld_inout_v8(p.residual + row + lc[v], rv[v][0], rv[v][1]);
+            else rv[v][0] = rv[v][1] = zero;
+            if (PRED || ok[v]) ld_stream_v8(p.x + row + lc[v], xv[v][0], xv[v][1]);
+            else xv[v][0] = xv[v][1] = zero;
+        } else {
 #pragma unroll
-        for (int c = 0; c < U; ++c) {
-            rv[v][c] = (p.residual && (PRED || ok[v])) ? ld_inout(p.residual + row + lc[v] + 8 * c) : zero;
-            xv[v][c] = (PRED || ok[v]) ? ld_stream(p.x + row + lc[v] + 8 * c) : zero;
+            for (int c = 0; c < U; ++c) {
+                rv[v][c] = (p.residual && (PRED || ok[v])) ? ld_inout(p.residual + row + lc[v] + 8 * c) : zero;
+                xv[v][c] = (PRED || ok[v]) ? ld_stream(p.x + row + lc[v] + 8 * c) : zero;
+            }
         }
+    }
     if (PARTS) {
         // a = dtype(((p0 + p1) + p2) + ...), fp32 accumulation in index order.
         // Partials are fetched four at a time so their loads are in flight
@@ -293,10 +318,16 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
             for (int j = 0; j < 4; ++j) {
                 const uint16_t *xp = p.x + (p0 + j) * p.part_stride + row;
 #pragma unroll
-                for (int v = 0; v < VPT; ++v)
+                for (int v = 0; v < VPT; ++v) {
+                    const bool ld = p0 + j < p.k && (PRED || ok[v]);
+                    if constexpr (V8) {
+                        if (ld) ld_stream_v8(xp + lc[v], pv[j][v][0], pv[j][v][1]);
+                        else pv[j][v][0] = pv[j][v][1] = zero;
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < U; ++c)
-                        pv[j][v][c] = (p0 + j < p.k && (PRED || ok[v])) ? ld_stream(xp + lc[v] + 8 * c) : zero;
+                        for (int c = 0; c < U; ++c) pv[j][v][c] = ld ? ld_stream(xp + lc[v] + 8 * c) : zero;
+                    }
+                }
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -319,10 +350,9 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
 #pragma unroll
             for (int c = 0; c < U; ++c) xv[v][c] = pack8<T>(&acc[v][8 * c]);
     }
-    if (!p.const_w) {
-        load_w();
-        qc = make_quant_ctx(p, MODE, es_smem, t, NT);
-    }
+    if constexpr (!EARLY) load_w();
+
+    const QuantCtx qc = EARLY ? qc_early : make_quant_ctx(p, MODE, es_smem, t, NT);
 
     // ---- h = dtype(a + residual), sum of squares ----
     uint4 hb[VPT][U];                        // packed h (the new residual)
@@ -372,10 +402,15 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     auto store_residual = [&]() {
         if (p.residual) {
 #pragma unroll
-            for (int v = 0; v < VPT; ++v)
+            for (int v = 0; v < VPT; ++v) {
+                if constexpr (V8) {
+                    st_v8_unit<PRED>(p.residual + row + col[v], hb[v][0], hb[v][1], ok[v]);
+                } else {
 #pragma unroll
-                for (int c = 0; c < U; ++c)
-                    st_v4_unit<PRED>(p.residual + row + col[v] + 8 * c, hb[v][c], ok[v]);
+                    for (int c = 0; c < U; ++c)
+                        st_v4_unit<PRED>(p.residual + row + col[v] + 8 * c, hb[v][c], ok[v]);
+                }
+            }
         }
     };
     if (C == 1) store_residual();
@@ -438,8 +473,8 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
                     }
                 }
             }
-            epilogue_unit<T, MODE, decltype(path)::value>(p, qc, yf, o, col[v],
-                                                          sf_col_offset(col[v]), ok[v], t);
+            epilogue_unit<T, MODE, decltype(path)::value, PRED, V8>(p, qc, yf, o, col[v],
+                                                                    sf_col_offset(col[v]), ok[v], t);
         }
     };
     if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
@@ -454,20 +489,20 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     __shared__ float es_smem[MODE == MODE_NVFP4 ? 256 : 1];
 
 // FP8, MXFP8 and no-quant rows: the compiler's own register choice.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL, int OPT>
 __global__ void __launch_bounds__(1024 / VPT) row_kernel(const __grid_constant__ Params p) {
     GNQ_ROW_SMEM
-    row_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, warp_ss, cta_ss, es_smem);
+    row_body<T, MODE, PARTS, VPT, LEAN, FULL, OPT>(p, warp_ss, cta_ss, es_smem);
 }
 
 // NVFP4 rows: the RowForm register budget (out-of-range units are
 // predicated, so there is no FULL instance).
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL, int OPT>
 __global__ void __launch_bounds__(1024 / VPT) __maxnreg__((RowForm<MODE, VPT, PARTS, LEAN>::maxnreg))
     row_kernel_nvfp4(const __grid_constant__ Params p) {
     static_assert(MODE == MODE_NVFP4 && !FULL, "NVFP4 rows only");
     GNQ_ROW_SMEM
-    row_body<T, MODE, PARTS, VPT, LEAN, false>(p, warp_ss, cta_ss, es_smem);
+    row_body<T, MODE, PARTS, VPT, LEAN, false, OPT>(p, warp_ss, cta_ss, es_smem);
 }
 #undef GNQ_ROW_SMEM
 
@@ -492,10 +527,12 @@ template <int MODE, int VPT, bool LEAN> struct StreamForm {
 };
 
 // FULL: the launch guarantees the row is exactly VPT units x threads.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
+// OPT_A32: the residual and y leave in 256-bit stores (NVFP4 units).
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL, int OPT>
 __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, float (*warp_ss)[32],
                                             float *es_smem, uint4 *topup) {
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
+    constexpr bool V8 = (OPT & OPT_A32) && U == 2;
     constexpr bool SW = StreamForm<MODE, VPT, LEAN>::smem_w;
     constexpr bool PRED = Pred<MODE>::value && !FULL;  // FULL: no unit is out of range
 
@@ -525,22 +562,17 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
         if (p.residual) bulk_g2s(dst + row_bytes * p.k, p.residual + m * p.H, row_bytes, bar);
     };
 
-    // wait for the preceding grid (its outputs may be this grid's inputs),
-    // then start the copies of the first rows
-    auto start_rows = [&]() {
-        pdl_wait();
-        pdl_trigger();
-        if (t == 0) {
-            for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
-        }
-    };
-    // The per-CTA constants below (the weight, packed if LEAN, else bias + w
-    // in fp32; the quantizer context) are read after that, or before it when
-    // the caller guarantees no preceding kernel writes w or the scale
-    // (const_w).
-    if (!p.const_w) start_rows();
+    pdl_wait();  // inputs may come from the preceding grid
+    pdl_trigger();
+
+    if (t == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int i = 0; i < n_rows && i < S; ++i) issue(i, i);
+    }
+
+    // per-CTA constants: the weight (packed if LEAN, else bias + w in fp32),
+    // quantizer context
     int col[VPT];
     bool ok[VPT];
     uint4 wq[VPT][LEAN ? U : 1];
@@ -578,8 +610,6 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
     }
     const uint32_t b16 = p.weight_bias == 1.f ? one16<T>() : 0u;  // LEAN: bias 1 or 0
     const QuantCtx qc = make_quant_ctx(p, MODE, es_smem, t, NT);
-
-    if (p.const_w) start_rows();
 
     __syncthreads();  // barriers initialised, table filled
 
@@ -630,6 +660,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
             float &acc_s = PRED ? sv : ss;
             uint64_t &acc_s2 = PRED ? sv2 : ss2;
             const bool ld = PRED || ok[v];
+            uint4 hr[U];  // the new residual of the unit (V8: stored once, below)
 #pragma unroll
             for (int c = 0; c < U; ++c) {
                 const uint32_t off = (uint32_t)(lc[v] + 8 * c) * 2u;
@@ -648,7 +679,8 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                 }
                 if (p.residual) {
                     xv = add16x8<T>(xv, ld ? lds_v4(stage + row_bytes * p.k + off) : zero);
-                    st_v4_unit<PRED>(p.residual + row + col[v] + 8 * c, xv, ok[v]);
+                    if constexpr (V8) hr[c] = xv;
+                    else st_v4_unit<PRED>(p.residual + row + col[v] + 8 * c, xv, ok[v]);
                 }
                 if constexpr (LEAN) {
                     hb[v][c] = xv;
@@ -662,6 +694,9 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                         acc_s2 = fma2(h2, h2, acc_s2);
                     }
                 }
+            }
+            if constexpr (V8) {
+                if (p.residual) st_v8_unit<PRED>(p.residual + row + col[v], hr[0], hr[1], ok[v]);
             }
             if constexpr (PRED) {
                 if constexpr (!LEAN) {
@@ -722,7 +757,7 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
                                  a[e], a[e + 1]);
                     }
                 }
-                epilogue_unit<T, MODE, decltype(path)::value, PRED>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
+                epilogue_unit<T, MODE, decltype(path)::value, PRED, V8>(p, qc, yf, o, col[v], sfc[v], ok[v], t);
             }
         };
         if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});
@@ -741,19 +776,19 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
     __shared__ __align__(16) uint4 topup[4];
 
 // FP8, MXFP8 and no-quant streaming: the compiler's own register choice.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL, int OPT>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) stream_kernel(const __grid_constant__ Params p) {
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem, topup);
+    stream_body<T, MODE, PARTS, VPT, LEAN, FULL, OPT>(p, dsmem, warp_ss, es_smem, topup);
 }
 
 // NVFP4 streaming: the StreamForm register budget.
-template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL>
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN, bool FULL, int OPT>
 __global__ void __launch_bounds__(VPT == 1 ? 1024 : 512) __maxnreg__((StreamForm<MODE, VPT, LEAN>::maxnreg))
     stream_kernel_nvfp4(const __grid_constant__ Params p) {
     static_assert(MODE == MODE_NVFP4, "NVFP4 streaming only");
     GNQ_STREAM_SMEM
-    stream_body<T, MODE, PARTS, VPT, LEAN, FULL>(p, dsmem, warp_ss, es_smem, topup);
+    stream_body<T, MODE, PARTS, VPT, LEAN, FULL, OPT>(p, dsmem, warp_ss, es_smem, topup);
 }
 #undef GNQ_STREAM_SMEM
 

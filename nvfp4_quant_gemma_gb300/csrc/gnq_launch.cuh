@@ -20,6 +20,7 @@ struct LaunchShape {
     bool pdl;        // launch as a programmatic dependent of the preceding grid
     bool lean;       // packed h / w form (fewest registers) instead of fp32 (fewest instructions)
     bool full;       // every unit of a CTA's segment in range (VPT x threads units)
+    int opt;         // OPT_* options of the instance
 };
 
 template <int MODE>
@@ -35,47 +36,86 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
 cudaError_t opt_in_dynamic_smem(const void *fn);
 
 // Resident CTAs per SM of the streaming kernel instance for this shape (0 on
-// error); opts the instance in to `smem` bytes of dynamic shared memory.
+// error); opts the instance in to its largest dynamic shared memory.
 template <int MODE>
 int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
                          size_t smem);
 
-#define GNQ_PICK_L(K, T, VPT, L, F)                                                   \
-    (parts ? (void (*)(const Params))K<T, MODE, true, VPT, L, F>                        \
-           : (void (*)(const Params))K<T, MODE, false, VPT, L, F>)
-#define GNQ_PICK(K, T, VPT, F) (lean ? GNQ_PICK_L(K, T, VPT, true, F) : GNQ_PICK_L(K, T, VPT, false, F))
+using KernelFn = void (*)(const Params);
 
-#define GNQ_PICK_VPT(K, T, F)                                                         \
-    (vpt == 1 ? GNQ_PICK(K, T, 1, F) : vpt == 2 ? GNQ_PICK(K, T, 2, F) : GNQ_PICK(K, T, 4, F))
-#define GNQ_PICK_T(K, F) (dtype == 0 ? GNQ_PICK_VPT(K, __nv_bfloat16, F) : GNQ_PICK_VPT(K, __half, F))
-
-// The kernel instance of a launch shape.  `full`: every unit of a CTA's
-// segment is in range; FP8 streaming, and NVFP4 streaming of one
-// activation, then run instances without per-unit checks (2.7 % and 3.0 %
-// faster on the fp16 16384 x 8192 no-residual batches; the same for the FP8
-// row kernel measured 4 % slower on the decode batch, for NVFP4 partials
-// 0.6 % slower).
-template <int MODE>
-void (*pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream, bool full))(const Params) {
+// The kernel instance of one launch.  Which instances exist:
+//   * `full` (every unit of a CTA's segment in range): FP8 streaming, and
+//     NVFP4 streaming of one activation, run instances without per-unit
+//     checks (2.7 % and 3.0 % faster on the fp16 16384 x 8192 no-residual
+//     batches; the same for the FP8 row kernel measured 4 % slower on the
+//     decode batch, for NVFP4 partials 0.6 % slower);
+//   * OPT_A32: NVFP4 instances that move a unit's 32-byte block in one
+//     256-bit access: row instances (which also exist without it, for
+//     tensors that are only 16-byte aligned), and the streaming instances
+//     of k partials, which store a residual and y (the host keeps such calls
+//     without 32-byte alignment on the row kernel).  The streaming
+//     instances of one activation -- under the automatic policy, batches
+//     that store neither -- keep the plain stores: the option changed their
+//     code and cost 2 % on the fp16 16384 x 8192 no-residual batch;
+//   * OPT_EARLYW: row instances of one unit per thread for one activation
+//     (the small batches, where reading the constants before the wait
+//     shortens the call).
+template <typename T, int MODE, bool PARTS, int VPT, bool LEAN>
+KernelFn pick_instance(bool stream, bool full, int opt) {
     if constexpr (MODE == MODE_NVFP4) {
-        // one activation only: with k partials the check-free instance was slower
-        if (stream)
-            return full && !parts ? GNQ_PICK_T(stream_kernel_nvfp4, true)
-                                  : GNQ_PICK_T(stream_kernel_nvfp4, false);
-        return GNQ_PICK_T(row_kernel_nvfp4, false);
-    } else if constexpr (MODE == MODE_FP8) {
-        if (stream) return full ? GNQ_PICK_T(stream_kernel, true) : GNQ_PICK_T(stream_kernel, false);
-        return GNQ_PICK_T(row_kernel, false);
+        if (stream) {
+            if constexpr (!PARTS) {
+                if (full) return stream_kernel_nvfp4<T, MODE, PARTS, VPT, LEAN, true, 0>;
+                return stream_kernel_nvfp4<T, MODE, PARTS, VPT, LEAN, false, 0>;
+            } else {
+                return stream_kernel_nvfp4<T, MODE, PARTS, VPT, LEAN, false, OPT_A32>;
+            }
+        }
+        if (opt & OPT_A32) {
+            if constexpr (VPT == 1 && !PARTS) {
+                if (opt & OPT_EARLYW)
+                    return row_kernel_nvfp4<T, MODE, PARTS, VPT, LEAN, false, OPT_A32 | OPT_EARLYW>;
+            }
+            return row_kernel_nvfp4<T, MODE, PARTS, VPT, LEAN, false, OPT_A32>;
+        }
+        return row_kernel_nvfp4<T, MODE, PARTS, VPT, LEAN, false, 0>;
     } else {
-        return stream ? GNQ_PICK_T(stream_kernel, false) : GNQ_PICK_T(row_kernel, false);
+        if (stream) {
+            if constexpr (MODE == MODE_FP8) {
+                if (full) return stream_kernel<T, MODE, PARTS, VPT, LEAN, true, 0>;
+            }
+            return stream_kernel<T, MODE, PARTS, VPT, LEAN, false, 0>;
+        }
+        if constexpr (VPT == 1 && !PARTS) {
+            if (opt & OPT_EARLYW) return row_kernel<T, MODE, PARTS, VPT, LEAN, false, OPT_EARLYW>;
+        }
+        return row_kernel<T, MODE, PARTS, VPT, LEAN, false, 0>;
     }
+}
+
+template <int MODE, typename T>
+KernelFn pick_typed(bool parts, int vpt, bool lean, bool stream, bool full, int opt) {
+#define GNQ_PICK(P, V, L) \
+    if (parts == P && vpt == V && lean == L) return pick_instance<T, MODE, P, V, L>(stream, full, opt);
+    GNQ_PICK(false, 1, false) GNQ_PICK(false, 1, true) GNQ_PICK(false, 2, false)
+    GNQ_PICK(false, 2, true) GNQ_PICK(false, 4, false) GNQ_PICK(false, 4, true)
+    GNQ_PICK(true, 1, false) GNQ_PICK(true, 1, true) GNQ_PICK(true, 2, false)
+    GNQ_PICK(true, 2, true) GNQ_PICK(true, 4, false) GNQ_PICK(true, 4, true)
+#undef GNQ_PICK
+    return nullptr;
+}
+
+template <int MODE>
+KernelFn pick_kernel(int dtype, bool parts, int vpt, bool lean, bool stream, bool full, int opt) {
+    return dtype == 0 ? pick_typed<MODE, __nv_bfloat16>(parts, vpt, lean, stream, full, opt)
+                      : pick_typed<MODE, __half>(parts, vpt, lean, stream, full, opt);
 }
 
 template <int MODE>
 int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, int threads,
                          size_t smem) {
-    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, vpt, lean, true, full);
-    if (opt_in_dynamic_smem(reinterpret_cast<const void *>(fn)) != cudaSuccess) return 0;
+    KernelFn fn = pick_kernel<MODE>(dtype, parts, vpt, lean, true, full, 0);
+    if (!fn || opt_in_dynamic_smem(reinterpret_cast<const void *>(fn)) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
         return 0;
@@ -85,7 +125,8 @@ int stream_blocks_per_sm(int dtype, bool parts, int vpt, bool lean, bool full, i
 template <int MODE>
 cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShape &ls,
                         cudaStream_t stream) {
-    void (*fn)(const Params) = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.lean, ls.stream, ls.full);
+    KernelFn fn = pick_kernel<MODE>(dtype, parts, ls.vpt, ls.lean, ls.stream, ls.full, ls.opt);
+    if (!fn) return cudaErrorInvalidConfiguration;
     if (ls.stream) {
         const cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void *>(fn));
         if (e != cudaSuccess) return e;
@@ -113,10 +154,5 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
     cfg.attrs = attr;
     return cudaLaunchKernelEx(&cfg, fn, p);
 }
-
-#undef GNQ_PICK_T
-#undef GNQ_PICK_VPT
-#undef GNQ_PICK
-#undef GNQ_PICK_L
 
 }  // namespace gnq

@@ -624,15 +624,16 @@ def test_bounded_wait_gives_up_and_the_next_call_is_clean(gnq):
     assert gnq.read_device_error() == 0
 
 
-@pytest.mark.parametrize("kernel", [1, 2])
+@pytest.mark.parametrize("M,kernel", [(100, 1), (300, 1), (300, 2)])
 @pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0), ("mxfp8", 0.0)])
-def test_constant_weights_flag(gnq, kernel, mode, scale):
-    """With the constant-weights flag the kernels read w and the scale before
-    they wait on the preceding kernel: single calls keep the parity contract,
-    and a dependent chain (each call consuming the residual the previous one
-    wrote) gives the bits of the default launches."""
+def test_constant_weights_flag(gnq, M, kernel, mode, scale):
+    """With the constant-weights flag, small batches (one unit per thread on
+    the row kernel, M = 100 here) read w and the scale before they wait on
+    the preceding kernel; other launches ignore it.  Single calls keep the
+    parity contract, and a dependent chain (each call consuming the residual
+    the previous one wrote) gives the bits of the default launches."""
     dev = torch.device("cuda")
-    x, r, w = _make(300, 4096, "bf16", seed=67)
+    x, r, w = _make(M, 4096, "bf16", seed=67)
     gnq.set_constant_weights(True)
     try:
         with forced_policy(gnq, kernel):
@@ -646,7 +647,10 @@ def test_constant_weights_flag(gnq, kernel, mode, scale):
         gnq.set_constant_weights(const_w)
         try:
             rd = r.to(dev)
-            outs = [gnq.alloc_outputs(300, 4096, mode, True, xd) for _ in range(4)]
+            outs = [gnq.alloc_outputs(M, 4096, mode, True, xd) for _ in range(4)]
+            for o in outs:  # NVFP4 scale rows M..round_up(M, 128) are never written
+                if o[1] is not None:
+                    o[1].view(torch.uint8).fill_(0xA5)
             with forced_policy(gnq, kernel):
                 for o in outs:
                     gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
@@ -658,3 +662,103 @@ def test_constant_weights_flag(gnq, kernel, mode, scale):
 
     assert all(torch.equal(a, b) for a, b in zip(chain(False), chain(True)))
     assert gnq.read_device_error() == 0
+
+
+@pytest.mark.parametrize("pdl", [True, False])
+@pytest.mark.parametrize("M", [64, 2048])
+def test_pdl_consumer_reads_the_finished_codes(gnq, pdl, M):
+    """The stand-in consumer (launched as a programmatic dependent of each
+    call, reading its own weight before it waits and the call's codes after)
+    sees every call's final codes, with the calls launched as programmatic
+    dependents or not: its checksum equals the one computed on the host from
+    the codes."""
+    dev = torch.device("cuda")
+    H, ctas = 5120, 40
+    x, r, w = _make(M, H, "bf16", seed=71)
+    xd, wd = x.to(dev), w.to(dev)
+    sd = torch.tensor([168.0], device=dev)
+    wt = torch.randint(0, 255, (ctas * 4096,), dtype=torch.uint8, device=dev)
+    outs, sums, rds = [], [], []
+    gnq.set_pdl(pdl)
+    try:
+        for i in range(3):
+            rd = r.to(dev)
+            o = gnq.alloc_outputs(M, H, "nvfp4", False, xd)
+            s_out = torch.zeros(ctas * 256, dtype=torch.int32, device=dev)
+            gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, "nvfp4", out=o)
+            gnq.pdl_consumer(o[0], wt, s_out, ctas)
+            outs.append(o)
+            sums.append(s_out)
+            rds.append(rd)
+        torch.cuda.synchronize()
+    finally:
+        gnq.set_pdl(True)
+
+    def host_checksum(q_bytes):
+        n_thr = ctas * 256
+        wv = wt.cpu().numpy().view(np.uint32).reshape(-1, 4)
+        wx = wv[:, 0] ^ wv[:, 1] ^ wv[:, 2] ^ wv[:, 3]
+        acc = np.zeros(n_thr, np.uint32)
+        for i0 in range(0, wx.size, n_thr):
+            seg = wx[i0:i0 + n_thr]
+            acc[:seg.size] ^= seg
+        qv = q_bytes.view(np.uint32).reshape(-1, 4)
+        qx = (qv[:, 0] ^ qv[:, 1] ^ qv[:, 2] ^ qv[:, 3]).astype(np.uint64)
+        acc = acc.astype(np.uint64)
+        for i0 in range(0, qx.size, n_thr):
+            seg = qx[i0:i0 + n_thr]
+            acc[:seg.size] += seg
+        return (acc & 0xFFFFFFFF).astype(np.uint32)
+
+    for o, s_out in zip(outs, sums):
+        want = host_checksum(u8(o[0]).reshape(-1))
+        assert np.array_equal(s_out.cpu().numpy().view(np.uint32), want)
+    run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=False, dtype="bf16")
+
+
+@pytest.mark.parametrize("kernel", [0, 1, 2])
+@pytest.mark.parametrize("M,H,k", [(200, 2048, 1), (700, 4096, 1), (90, 1024, 3)])
+def test_nvfp4_16_byte_aligned_buffers(gnq, kernel, M, H, k):
+    """NVFP4 calls whose 16-bit tensors are 16-byte but not 32-byte aligned
+    (views 8 elements into larger buffers) take the instances without
+    256-bit accesses -- the row kernel, whatever shape is forced -- and give
+    the bits of the same call on 32-byte aligned buffers."""
+    dev = torch.device("cuda")
+    x, r, w = _make(M, H, "bf16", seed=73, k=k)
+    sd = torch.tensor([168.0], device=dev)
+
+    def off16(t):
+        buf = torch.empty(t.numel() + 8, dtype=t.dtype, device=dev)
+        v = buf[8:].view(t.shape)
+        v.copy_(t.to(dev))
+        assert v.data_ptr() % 32 == 16
+        return v
+
+    results = []
+    for place in (lambda t: t.to(dev).clone(), off16):
+        xd, rd, wd = place(x), place(r), place(w)
+        yb = torch.empty(M * H + 8, dtype=torch.bfloat16, device=dev)
+        y = yb[8:].view(M, H) if place is off16 else yb[:M * H].view(M, H)
+        q, bs, _ = gnq.alloc_outputs(M, H, "nvfp4", False, xd)
+        bs.view(torch.uint8).fill_(0xA5)
+        with forced_policy(gnq, kernel):
+            if k > 1:
+                gnq.gemma_add_rms_norm_quant_parts(xd, rd, wd, 1e-6, sd, "nvfp4", write_y=True,
+                                                   out=(q, bs, y))
+            else:
+                gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, "nvfp4", write_y=True,
+                                             out=(q, bs, y))
+        torch.cuda.synchronize()
+        results.append([rd.cpu(), y.cpu(), q.cpu(), bs.view(torch.uint8).cpu()])
+    (r_a, y_a, q_a, s_a), (r_b, y_b, q_b, s_b) = results
+    assert torch.equal(r_a, r_b)
+    if kernel != 2:
+        # the same launch shape on both sides: the same bits everywhere
+        assert torch.equal(y_a, y_b) and torch.equal(q_a, q_b) and torch.equal(s_a, s_b)
+    else:
+        # the forced streaming shape fell back to the row kernel on the
+        # misaligned side, which sums the squares in another order
+        assert int(ulp_distance16(bits(y_a), bits(y_b)).max()) <= 1
+    # and the misaligned call passes the whole contract against the oracle
+    with forced_policy(gnq, kernel):
+        run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
