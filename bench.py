@@ -289,8 +289,11 @@ class Case:
         return g
 
 
-def time_graph(g, dev, n_steps: int, barrier=None, soak_s: float = 0.0, sampler=None):
-    """Replay g once inside CUDA events (after optional soak replays)."""
+def time_graph(g, dev, n_steps: int, barrier=None, soak_s: float = 0.0, sampler=None,
+               profile_range: bool = False):
+    """Replay g once inside CUDA events (after optional soak replays).  With
+    profile_range the timed replay is also bracketed by cudaProfilerStart /
+    Stop, so a profiler started with profiling off captures exactly it."""
     stream = torch.cuda.current_stream(dev)
     ctx = sampler if sampler is not None else _Null()
     with ctx:
@@ -303,10 +306,14 @@ def time_graph(g, dev, n_steps: int, barrier=None, soak_s: float = 0.0, sampler=
         torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        if profile_range:
+            torch.cuda.profiler.start()
         e0.record(stream)
         g.replay()
         e1.record(stream)
         torch.cuda.synchronize(dev)
+        if profile_range:
+            torch.cuda.profiler.stop()
         if barrier:
             barrier()
         ms = e0.elapsed_time(e1)
@@ -609,7 +616,8 @@ def run_gnq(args, rank: int, world: int, barrier):
     g_warm.replay()
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(device_uuid(dev)) if rank == 0 else None
-    ms = time_graph(g_timed, dev, args.steps, barrier=barrier, soak_s=args.soak, sampler=sampler)
+    ms = time_graph(g_timed, dev, args.steps, barrier=barrier, soak_s=args.soak, sampler=sampler,
+                    profile_range=True)
     ms_max = max_over_ranks(ms, world, dev)
     bytes_step = wl.algorithmic_bytes()
     value = bytes_step * args.steps * world / (ms_max / 1e3) / 1e9
