@@ -736,15 +736,19 @@ def workload_table(gnq, dev, l2, peak):
     return rows
 
 
-# launch shapes compared by the small-batch sweep: (label, kernel, cluster)
-SWEEP_SHAPES = (("auto", 0, 0), ("row_cluster2", 1, 2), ("row_cluster4", 1, 4), ("stream", 2, 0))
+# launch shapes compared by the small-batch sweep: (label, kernel, cluster); for
+# the streaming kernel `cluster` is the least number of rows per CTA
+SWEEP_SHAPES = (("auto", 0, 0), ("row_cluster2", 1, 2), ("row_cluster4", 1, 4), ("stream", 2, 0),
+                ("stream_2rows", 2, 2))
 
 
 def small_m_sweep(gnq, dev, l2, peak, modes=("fp8", "nvfp4"), m_values=SMALL_M):
     """Latency for M = 1 .. 8192 rows at H = 5120 (bf16, residual, y), in the
     static-FP8 and the NVFP4 mode: the automatic launch shape against
     split-row clusters of 2 and 4 CTAs (partial sums of squares exchanged
-    through distributed shared memory) and the persistent streaming grid."""
+    through distributed shared memory), the persistent streaming grid, and
+    that grid with at least two rows per CTA (the second row's copy in
+    flight while the first is computed)."""
     rows = []
     try:
         for mode in modes:

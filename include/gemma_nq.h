@@ -171,7 +171,10 @@ const char *gnq_status_string(int status);
  * Tuning hook: force the launch shape of later calls in this process.
  *   kernel   0 = automatic; 1 = one CTA (or cluster) per row; 2 = persistent
  *            streaming kernel (rows staged through shared memory).
- *   cluster  row kernel only: 0 = automatic, else 1, 2, 4 or 8 CTAs per row.
+ *   cluster  row kernel: 0 = automatic, else 1, 2, 4 or 8 CTAs per row.
+ *            Streaming kernel: 0 = automatic grid, else at least that many
+ *            rows (2, 4 or 8) per CTA (grid = ceil(M / cluster) CTAs when
+ *            that is below one wave).
  *   vpt      0 = automatic, else 1, 2 or 4 units (8 elements; 16 for
  *            NVFP4) per thread.
  *   form     0 = automatic; 1 = h and the weight unpacked to fp32 (fewest

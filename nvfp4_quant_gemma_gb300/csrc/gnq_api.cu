@@ -1,6 +1,7 @@
 // C ABI of the fused add + Gemma RMSNorm + quant library: argument checks,
 // launch-shape policy and dispatch.  The contract of every entry point is in
 // include/gemma_nq.h.
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -269,11 +270,16 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     if (fk) stream = fk == 2;
     if (!allow_stream) stream = false;
     if (fv) vpt = fv;
+    // a forced streaming launch may ask for at least `fc` rows per CTA
+    auto rows_per_cta = [&](LaunchShape &l) {
+        if (fk == 2 && fc > 1) l.grid = std::min<int64_t>(l.grid, (M + fc - 1) / fc);
+        return true;
+    };
     if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls))
-        return ls;
+        return rows_per_cta(ls), ls;
     if (stream &&
         stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256)), ls))
-        return ls;
+        return rows_per_cta(ls), ls;
 
     ls.vpt = fv ? fv : (stream ? 1 : vpt);
     const int64_t gran2 = 2LL * granule(mode);

@@ -63,14 +63,21 @@ struct QuantCtx {
     const float *es_tab;  // NVFP4: element scale g / value(sf) per sf code (shared memory)
 };
 
-// Fill the NVFP4 element-scale table: RN(g / value(code)), 0 for a zero scale.
-__device__ __forceinline__ void fill_es_table(float *tab, float g, int t, int nt) {
-    for (int c = t; c < 256; c += nt) {
-        const float v = e4m3_value((uint32_t)c);
-        tab[c] = v == 0.f ? 0.f : __fdiv_rn(g, v);
-    }
+// NVFP4 element scale of a block-scale code: RN(g / value(code)), 0 for a
+// zero scale.
+__device__ __forceinline__ float element_scale(float g, uint32_t code) {
+    const float v = e4m3_value(code);
+    return v == 0.f ? 0.f : __fdiv_rn(g, v);
 }
 
+// Fill the NVFP4 element-scale table for all 256 codes.
+__device__ __forceinline__ void fill_es_table(float *tab, float g, int t, int nt) {
+    for (int c = t; c < 256; c += nt) tab[c] = element_scale(g, (uint32_t)c);
+}
+
+// TABLE: NVFP4 blocks look their element scale up in a per-CTA table (else
+// each block divides once; see row_body).
+template <bool TABLE = true>
 __device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, float *es_smem,
                                                    int t, int nt) {
     QuantCtx qc;
@@ -80,7 +87,7 @@ __device__ __forceinline__ QuantCtx make_quant_ctx(const Params &p, int mode, fl
     if (mode == MODE_FP8) qc.fd = make_fp8_div(__ldg(p.scale));
     if (mode == MODE_NVFP4) {
         qc.g = __ldg(p.scale);
-        fill_es_table(es_smem, qc.g, t, nt);  // visible after the next __syncthreads
+        if (TABLE) fill_es_table(es_smem, qc.g, t, nt);  // visible after the next __syncthreads
     }
     return qc;
 }
@@ -142,8 +149,10 @@ template <bool PRED> __device__ __forceinline__ void st_u8_unit(void *p, uint32_
 // FP8PATH is the FP8 quotient path (FP8_*), uniform per CTA; `sfc` is the
 // unit's sf_col_offset (NVFP4).  PRED: out-of-range units are predicated
 // (Pred<MODE>), unless the instance has none (FULL).  V8: the two chunks of
-// an NVFP4 unit's y leave in one 256-bit store (32-byte aligned y).
-template <typename T, int MODE, int FP8PATH, bool PRED = Pred<MODE>::value, bool V8 = false>
+// an NVFP4 unit's y leave in one 256-bit store (32-byte aligned y).  ESDIV:
+// the NVFP4 element scale is divided out per block instead of looked up.
+template <typename T, int MODE, int FP8PATH, bool PRED = Pred<MODE>::value, bool V8 = false,
+          bool ESDIV = false>
 __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &qc,
                                               float (&yf)[Unit<MODE>::E], const RowOut &o,
                                               int col, int sfc, bool ok, int t) {
@@ -180,7 +189,7 @@ __device__ __forceinline__ void epilogue_unit(const Params &p, const QuantCtx &q
         const uint32_t sf = e4m3x2(sf32, 0.f) & 0xFF;
         Act<T>::unpack(yb[0], &yf[0]);
         Act<T>::unpack(yb[1], &yf[8]);
-        mul_arr_s<16>(yf, qc.es_tab[sf]);
+        mul_arr_s<16>(yf, ESDIV ? element_scale(qc.g, sf) : qc.es_tab[sf]);
         const uint32_t lo = e2m1x8(&yf[0]);
         const uint32_t hi = e2m1x8(&yf[8]);
         st_v2_unit<PRED>(o.q + (col >> 1), lo, hi, ok);
@@ -243,6 +252,12 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     constexpr int U = Unit<MODE>::U, E = Unit<MODE>::E;
     constexpr bool V8 = (OPT & OPT_A32) && U == 2;
     constexpr bool EARLY = (OPT & OPT_EARLYW) != 0;
+    // NVFP4 at one unit per thread (the small batches, bound by latency):
+    // one division per block instead of a 256-entry table per CTA, which
+    // would sit between the scale's load and the first block's codes (M = 1,
+    // H = 5120: 1.80 -> 1.68 us).  With EARLY the table is built before the
+    // wait and its lookup is the shorter path (1.59 us).
+    constexpr bool ESDIV = MODE == MODE_NVFP4 && VPT == 1 && !EARLY;
 
     const uint32_t C = cluster_size();
     const uint32_t rank = C > 1 ? cluster_rank() : 0;
@@ -281,7 +296,7 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     QuantCtx qc_early{};
     if constexpr (EARLY) {  // constants first, then the wait on the preceding grid
         load_w();
-        qc_early = make_quant_ctx(p, MODE, es_smem, t, NT);
+        qc_early = make_quant_ctx<!ESDIV>(p, MODE, es_smem, t, NT);
     }
 
     pdl_wait();  // inputs may come from the preceding grid
@@ -352,7 +367,7 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
     }
     if constexpr (!EARLY) load_w();
 
-    const QuantCtx qc = EARLY ? qc_early : make_quant_ctx(p, MODE, es_smem, t, NT);
+    const QuantCtx qc = EARLY ? qc_early : make_quant_ctx<!ESDIV>(p, MODE, es_smem, t, NT);
 
     // ---- h = dtype(a + residual), sum of squares ----
     uint4 hb[VPT][U];                        // packed h (the new residual)
@@ -473,8 +488,8 @@ __device__ __forceinline__ void row_body(const Params &p, float *warp_ss, float 
                     }
                 }
             }
-            epilogue_unit<T, MODE, decltype(path)::value, PRED, V8>(p, qc, yf, o, col[v],
-                                                                    sf_col_offset(col[v]), ok[v], t);
+            epilogue_unit<T, MODE, decltype(path)::value, PRED, V8, ESDIV>(
+                p, qc, yf, o, col[v], sf_col_offset(col[v]), ok[v], t);
         }
     };
     if (MODE == MODE_FP8 && !qc.fd.fast) finish(std::integral_constant<int, FP8_IEEE>{});

@@ -246,11 +246,12 @@ class forced_policy:
 
 
 @pytest.mark.parametrize("kernel,cluster,vpt", [(1, c, v) for c in (1, 2, 4, 8) for v in (1, 2, 4)]
-                         + [(2, 0, v) for v in (1, 2, 4)])
+                         + [(2, 0, v) for v in (1, 2, 4)] + [(2, r, 2) for r in (2, 8)])
 @pytest.mark.parametrize("form", [1, 2])
 def test_every_launch_shape(gnq, kernel, cluster, vpt, form):
-    """Forced kernels, cluster sizes, units per thread and register forms
-    give the same contract."""
+    """Forced kernels, cluster sizes (for the streaming kernel: at least that
+    many rows per CTA), units per thread and register forms give the same
+    contract."""
     x, r, w = _make(133, 4096, "bf16", seed=cluster * 10 + vpt + kernel)
     with forced_policy(gnq, kernel, cluster, vpt, form):
         run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
@@ -762,3 +763,18 @@ def test_nvfp4_16_byte_aligned_buffers(gnq, kernel, M, H, k):
     # and the misaligned call passes the whole contract against the oracle
     with forced_policy(gnq, kernel):
         run_case(gnq, x, r, w, "nvfp4", 168.0, write_y=True, dtype="bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.08), ("nvfp4", 84.0), ("mxfp8", 0.0)])
+@pytest.mark.parametrize("M,H", [(700, 8192), (333, 8192 + 64), (160, 2048)])
+def test_streaming_without_residual_or_y(gnq, dtype, mode, scale, M, H):
+    """The streaming instances compiled for launches with neither a residual
+    nor y (four units per thread, packed form), on rows that are and are not
+    a whole number of units per thread: the call without y must give the
+    codes of the same launch shape writing y (a generic instance), and the
+    whole contract against the oracle."""
+    x, _, w = _make(M, H, dtype, seed=M + 3, residual=False)
+    with forced_policy(gnq, 2, 0, 4, 2):
+        run_case(gnq, x, None, w, mode, scale, write_y=False, dtype=dtype)
+    assert gnq.read_device_error() == 0
