@@ -332,12 +332,13 @@ class _Null:
         pass
 
 
-def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None, graph: bool = True):
+def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None, graph: bool = True,
+                n_lanes: int = 2):
     """Same metric through the public API with host buffers: every step copies
     its inputs from pinned host memory, runs the op, and reads its results
-    back into pinned host memory.  Steps alternate between two streams with
+    back into pinned host memory.  Steps rotate over `n_lanes` streams with
     their own device buffers, so one step's copy back overlaps the next
-    step's copy in (separate copy engines) and compute.  With `graph` the
+    steps' copies in (separate copy engines) and compute.  With `graph` the
     steps' copies and calls are captured once into a CUDA graph and replayed
     (as a serving loop would), which removes the per-call host overhead but
     none of the transfers; otherwise they are issued eagerly."""
@@ -351,7 +352,7 @@ def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None, graph: bool
     w = inp["weight"].to(dev)
     s = inp["scale"].to(dev)
     lanes = []
-    for _ in range(2):
+    for _ in range(n_lanes):
         xd = torch.empty_like(inp["x"], device=dev)
         rd = None if inp["residual"] is None else torch.empty_like(inp["residual"], device=dev)
         out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, wl.write_y, xd)
@@ -364,7 +365,7 @@ def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None, graph: bool
     d2h += 0 if lanes[0][5] is None else lanes[0][5].numel() * lanes[0][5].element_size()
 
     def one(i):
-        st, xd, rd, out, host_out, host_r = lanes[i % 2]
+        st, xd, rd, out, host_out, host_r = lanes[i % n_lanes]
         hx, hr = host_in[i % n_host]
         with torch.cuda.stream(st):
             xd.copy_(hx, non_blocking=True)
