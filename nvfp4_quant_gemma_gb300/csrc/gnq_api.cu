@@ -270,16 +270,13 @@ LaunchShape choose_shape(const DevInfo &d, int64_t M, int64_t H, int mode, int d
     if (fk) stream = fk == 2;
     if (!allow_stream) stream = false;
     if (fv) vpt = fv;
-    // a forced streaming launch may ask for at least `fc` rows per CTA
-    auto rows_per_cta = [&](LaunchShape &l) {
-        if (fk == 2 && fc > 1) l.grid = std::min<int64_t>(l.grid, (M + fc - 1) / fc);
-        return true;
-    };
-    if (stream && stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls))
-        return rows_per_cta(ls), ls;
-    if (stream &&
-        stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256)), ls))
-        return rows_per_cta(ls), ls;
+    if (stream && (stream_shape(d, M, H, mode, dtype, k, nops, vpt, lean_for(vpt), ls) ||
+                   stream_shape(d, M, H, mode, dtype, k, nops, vpt_for(256), lean_for(vpt_for(256)),
+                                ls))) {
+        // a forced streaming launch may ask for at least `fc` rows per CTA
+        if (fk == 2 && fc > 1) ls.grid = std::min<int64_t>(ls.grid, (M + fc - 1) / fc);
+        return ls;
+    }
 
     ls.vpt = fv ? fv : (stream ? 1 : vpt);
     const int64_t gran2 = 2LL * granule(mode);
