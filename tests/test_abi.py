@@ -114,6 +114,33 @@ def test_query_launch_validation(lib):
     assert call() in (0, 7)                    # valid: a shape, or no device here
 
 
+def test_switches_and_diagnostics_validate_their_arguments(lib):
+    """The process-wide switches accept only their documented values, the
+    tuning hook only its documented sets, and the stand-in consumer rejects
+    bad sizes and missing buffers -- all on the host, before any CUDA call.
+    Valid switch values are restored to the defaults afterwards."""
+    P = ctypes.c_void_p
+    for fn in (lib.gnq_set_pdl, lib.gnq_set_constant_weights, lib.gnq_inject_wait_timeout):
+        assert fn(2) == 2 and fn(-1) == 2
+        assert fn(0) == 0
+    assert lib.gnq_set_pdl(1) == 0                              # back to the default
+    assert lib.gnq_set_launch_policy(3, 0, 0, 0) == 2            # kernel
+    assert lib.gnq_set_launch_policy(2, 3, 0, 0) == 2            # rows per CTA not a power of 2
+    assert lib.gnq_set_launch_policy(2, 16, 0, 0) == 2           # more than 8
+    assert lib.gnq_set_launch_policy(1, 0, 3, 0) == 2            # units per thread
+    assert lib.gnq_set_launch_policy(1, 0, 0, 3) == 2            # form
+    assert lib.gnq_set_launch_policy(2, 2, 0, 0) == 0            # streaming, >= 2 rows per CTA
+    assert lib.gnq_set_launch_policy(0, 0, 0, 0) == 0
+    c = lib.gnq_pdl_consumer
+    i64 = ctypes.c_int64
+    buf = P(4096)  # never dereferenced: every call below is rejected first
+    assert c(buf, i64(24), buf, i64(16), buf, 1, None) == 2      # q bytes not a multiple of 16
+    assert c(buf, i64(16), buf, i64(-16), buf, 1, None) == 2     # negative weight bytes
+    assert c(buf, i64(16), buf, i64(16), buf, 0, None) == 2      # no CTA
+    assert c(buf, i64(16), buf, i64(16), None, 1, None) == 1     # no output
+    assert c(None, i64(16), buf, i64(16), buf, 1, None) == 1     # no codes
+
+
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
     from nvfp4_quant_gemma_gb300 import _binding, build
     monkeypatch.setattr(build, "LIB", str(tmp_path / "missing.so"))
