@@ -26,16 +26,13 @@
 // Each exists as two __global__ wrappers around one inlined body: the
 // FP8 / MXFP8 / no-quant instances (register choice left to the compiler)
 // and the *_nvfp4 instances (explicit register budgets, RowForm and
-// StreamForm).  Instance options are template arguments (OPT bits, see
-// gnq_device.cuh), never runtime branches: a branch that is never taken
-// still changes register allocation and instruction order of the whole
-// body.
+// StreamForm).
 //
 // Work inside a CTA: a thread owns VPT units of U contiguous 16-byte chunks
 // (8U elements; U = 2 for NVFP4, so a thread holds whole 16-element blocks,
 // else U = 1), unit u = v * blockDim.x + threadIdx.x, so a warp-wide access
-// is one contiguous line (with OPT_A32 an NVFP4 unit moves in one 256-bit
-// access).  Everything between the load and the stores stays in registers.  The sum of squares is an fp32 warp shuffle tree, then a
+// is one contiguous line.  Everything between the load and the stores stays
+// in registers.  The sum of squares is an fp32 warp shuffle tree, then a
 // second shuffle tree over the per-warp partials, the same in every warp.
 // Every rounding that decides a code is an IEEE round-to-nearest operation
 // (see gnq_device.cuh), so codes are exactly those of the fp32 reading.
