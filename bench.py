@@ -698,6 +698,7 @@ def run_gnq(args, rank: int, world: int, barrier):
     if world == 1 and not args.no_sweep:
         line["small_m_sweep"] = small_m_sweep(gnq, dev, l2, peak)
         line["pdl_consumer_sweep"] = pdl_consumer_sweep(gnq, dev, l2)
+        line["dependent_launch_floor"] = dependent_launch_floor(gnq, dev)
     return line
 
 
@@ -838,6 +839,31 @@ def pdl_consumer_sweep(gnq, dev, l2, modes=("fp8", "nvfp4"), m_values=PDL_M):
     finally:
         gnq.set_pdl(True)
     return rows
+
+
+def dependent_launch_floor(gnq, dev, n: int = 2000) -> dict:
+    """Time per kernel of a chain of n programmatic dependents that move
+    almost nothing (the stand-in consumer, one CTA, reading 16 bytes after
+    its wait): the launch-and-dependency cost any dependent call pays on
+    this GPU before it moves data."""
+    q = torch.zeros(16, dtype=torch.uint8, device=dev)
+    no_weight = torch.empty(0, dtype=torch.uint8, device=dev)
+    out = torch.empty(256, dtype=torch.int32, device=dev)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        gnq.pdl_consumer(q, no_weight, out, 1)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.graph(g):
+        for _ in range(n):
+            gnq.pdl_consumer(q, no_weight, out, 1)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    return {"us_per_kernel": round(time_graph(g, dev, n) / n * 1e3, 3), "kernels": n,
+            "how": "a CUDA graph of dependent launches of the stand-in consumer (one CTA, "
+                   "16 bytes read after its wait, nothing before it), CUDA events"}
 
 
 # ----------------------------------------------------------------------------
