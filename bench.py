@@ -332,16 +332,37 @@ class _Null:
         pass
 
 
+def row_blocks(M: int, chunks: int) -> list[tuple[int, int]]:
+    """Split M rows into at most `chunks` consecutive blocks whose starts are
+    multiples of 128 rows (so an NVFP4 block-scale buffer splits at 128-row
+    tile boundaries into contiguous pieces)."""
+    per = -(-(-(-M // max(1, chunks))) // 128) * 128
+    bounds, a = [], 0
+    while a < M:
+        bounds.append((a, min(M, a + per)))
+        a += per
+    return bounds
+
+
 def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None, graph: bool = True,
-                n_lanes: int = 2):
+                chunks: int = 4, n_sets: int = 2, results: list | None = None, reps: int = 3,
+                times: list | None = None):
     """Same metric through the public API with host buffers: every step copies
     its inputs from pinned host memory, runs the op, and reads its results
-    back into pinned host memory.  Steps rotate over `n_lanes` streams with
-    their own device buffers, so one step's copy back overlaps the next
-    steps' copies in (separate copy engines) and compute.  With `graph` the
-    steps' copies and calls are captured once into a CUDA graph and replayed
-    (as a serving loop would), which removes the per-call host overhead but
-    none of the transfers; otherwise they are issued eagerly."""
+    back into pinned host memory.  A step's rows are cut into `chunks` row
+    blocks (the op is row-wise); each block goes host -> device on a copy-in
+    stream, through the op on a compute stream, and back on a copy-out
+    stream, so the link carries both directions at once while the op runs on
+    the blocks in between, across step boundaries too.  Device buffers and
+    host result buffers rotate over `n_sets` sets; a block of a set is copied
+    in again only after its previous results have been copied out.  With
+    `graph` the steps are captured once into a CUDA graph and replayed (as a
+    serving loop would), which removes the per-call host overhead but none of
+    the transfers; otherwise they are issued eagerly.  The `steps` are timed
+    `reps` times (the host link is shared with the machine's other work) and
+    the median is returned; `times`, if given, receives every run's ms.
+    `results`, if given, receives each set's host results ((q, block_scale,
+    y), residual) after the timed steps, for checking."""
     inp = make_inputs(wl)
     n_host = 4
     host_in = []
@@ -351,82 +372,121 @@ def e2e_measure(gnq, wl, dev, steps: int, warmup: int, barrier=None, graph: bool
         host_in.append((x, r))
     w = inp["weight"].to(dev)
     s = inp["scale"].to(dev)
-    lanes = []
-    for _ in range(n_lanes):
+    row_dim = 1 if wl.k > 1 else 0  # x_parts is (k, M, H)
+    sets = []
+    for _ in range(n_sets):
         xd = torch.empty_like(inp["x"], device=dev)
         rd = None if inp["residual"] is None else torch.empty_like(inp["residual"], device=dev)
         out = gnq.alloc_outputs(wl.M, wl.H, wl.mode, wl.write_y, xd)
         host_out = [None if t is None else torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                     for t in out]
         host_r = None if rd is None else torch.empty(rd.shape, dtype=rd.dtype, pin_memory=True)
-        lanes.append((torch.cuda.Stream(dev), xd, rd, out, host_out, host_r))
+        sets.append((xd, rd, out, host_out, host_r))
     h2d = sum(t.numel() * t.element_size() for t in host_in[0] if t is not None)
-    d2h = sum(t.numel() * t.element_size() for t in lanes[0][4] if t is not None)
-    d2h += 0 if lanes[0][5] is None else lanes[0][5].numel() * lanes[0][5].element_size()
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][3] if t is not None)
+    d2h += 0 if sets[0][4] is None else sets[0][4].numel() * sets[0][4].element_size()
+    # k partials: one block (a row slice of (k, M, H) is not one contiguous tensor)
+    bounds = row_blocks(wl.M, chunks if wl.k == 1 else 1)
+    s_in, s_op, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    free = {}  # (set, block) -> event after that block's results were copied out
+
+    def rows(t, a, e, dim=0):
+        return t.narrow(dim, a, e - a)
 
     def one(i):
-        st, xd, rd, out, host_out, host_r = lanes[i % n_lanes]
+        b = i % n_sets
         hx, hr = host_in[i % n_host]
-        with torch.cuda.stream(st):
-            xd.copy_(hx, non_blocking=True)
-            if rd is not None:
-                rd.copy_(hr, non_blocking=True)
-            if wl.k > 1:
-                gnq.gemma_add_rms_norm_quant_parts(xd, rd, w, wl.eps, s, wl.mode,
-                                                   write_y=wl.write_y, out=out)
-            else:
-                gnq.gemma_add_rms_norm_quant(xd, rd, w, wl.eps, s, wl.mode,
-                                             write_y=wl.write_y, out=out)
-            for h, d in zip(host_out, out):
-                if h is not None:
-                    h.copy_(d, non_blocking=True)
-            if rd is not None:
-                host_r.copy_(rd, non_blocking=True)
+        xd, rd, out, host_out, host_r = sets[b]
+        for j, (a, e) in enumerate(bounds):
+            if (b, j) in free:
+                s_in.wait_event(free[(b, j)])
+            with torch.cuda.stream(s_in):
+                rows(xd, a, e, row_dim).copy_(rows(hx, a, e, row_dim), non_blocking=True)
+                if rd is not None:
+                    rows(rd, a, e).copy_(rows(hr, a, e), non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_in)
+            s_op.wait_event(ev)
+            q, bs, y = out
+            # the block's outputs: NVFP4 scales in whole 128-row tiles
+            bs_e = bs.shape[0] if (bs is not None and wl.mode == "nvfp4" and e == wl.M) else e
+            o = (None if q is None else rows(q, a, e),
+                 None if bs is None or wl.mode == "fp8" else rows(bs, a, bs_e),
+                 None if y is None else rows(y, a, e))
+            xs, rs = rows(xd, a, e, row_dim), None if rd is None else rows(rd, a, e)
+            with torch.cuda.stream(s_op):
+                if wl.k > 1:
+                    gnq.gemma_add_rms_norm_quant_parts(xs, rs, w, wl.eps, s, wl.mode,
+                                                       write_y=wl.write_y, out=o)
+                else:
+                    gnq.gemma_add_rms_norm_quant(xs, rs, w, wl.eps, s, wl.mode,
+                                                 write_y=wl.write_y, out=o)
+            ev = torch.cuda.Event()
+            ev.record(s_op)
+            s_out.wait_event(ev)
+            with torch.cuda.stream(s_out):
+                for h, d in zip(host_out, o):
+                    if d is not None:
+                        hs = rows(h, a, bs_e) if d is o[1] else rows(h, a, e)
+                        hs.copy_(d, non_blocking=True)
+                if rd is not None:
+                    rows(host_r, a, e).copy_(rs, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(s_out)
+            free[(b, j)] = ev
 
-    def run_steps(origin):
-        # both lanes start after `origin`; `origin` then waits for both
-        for lane in lanes:
-            lane[0].wait_stream(origin)
-        for i in range(steps):
+    def run_steps(origin, n):
+        # every stream starts after `origin`; `origin` then waits for all
+        free.clear()
+        for st in (s_in, s_op, s_out):
+            st.wait_stream(origin)
+        for i in range(n):
             one(i)
-        for lane in lanes:
-            origin.wait_stream(lane[0])
+        for st in (s_in, s_op, s_out):
+            origin.wait_stream(st)
 
-    for i in range(warmup):
-        one(i)
-    torch.cuda.synchronize(dev)
     main = torch.cuda.current_stream(dev)
+    run_steps(main, warmup)
+    torch.cuda.synchronize(dev)
     g = None
     if graph:
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(main)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
-            run_steps(cap)
+            run_steps(cap, steps)
         main.wait_stream(cap)
         g.replay()  # warm replay
         torch.cuda.synchronize(dev)
-    if barrier:
-        barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(main)
-    if g is not None:
-        g.replay()
-    else:
-        run_steps(main)
-    e1.record(main)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1)
-    return ms, h2d, d2h
+    runs = []
+    for _ in range(max(1, reps)):
+        if barrier:
+            barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        if g is not None:
+            g.replay()
+        else:
+            run_steps(main, steps)
+        e1.record(main)
+        torch.cuda.synchronize(dev)
+        runs.append(e0.elapsed_time(e1))
+    if times is not None:
+        times.extend(runs)
+    if results is not None:
+        results.extend((st[3], st[4]) for st in sets)
+    return statistics.median(runs), h2d, d2h
 
 
-def e2e_zero_copy(gnq, wl, dev, steps: int, warmup: int, l2_bytes: int, barrier=None):
+def e2e_zero_copy(gnq, wl, dev, steps: int, warmup: int, l2_bytes: int, barrier=None,
+                  reps: int = 3):
     """Same metric with every buffer in pinned host memory: each step's
     kernel reads its inputs and writes its results through the host link
     (NVLink-C2C on a Grace-Blackwell node) with no separate copy.  Enough host
     sets rotate that their total is over 2.5x L2, so no step finds its inputs
-    cached; the steps are captured in a CUDA graph and replayed."""
+    cached; the steps are captured in a CUDA graph and replayed, `reps` times
+    (the median is returned)."""
     inp = make_inputs(wl)
     per_set = wl.algorithmic_bytes()
     n_sets = max(2, min(64, math.ceil(2.5 * l2_bytes / per_set)))
@@ -464,21 +524,26 @@ def e2e_zero_copy(gnq, wl, dev, steps: int, warmup: int, l2_bytes: int, barrier=
     main.wait_stream(cap)
     g.replay()
     torch.cuda.synchronize(dev)
-    if barrier:
-        barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(main)
-    g.replay()
-    e1.record(main)
-    torch.cuda.synchronize(dev)
-    return e0.elapsed_time(e1), h2d, d2h
+    runs = []
+    for _ in range(max(1, reps)):
+        if barrier:
+            barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        g.replay()
+        e1.record(main)
+        torch.cuda.synchronize(dev)
+        runs.append(e0.elapsed_time(e1))
+    return statistics.median(runs), h2d, d2h
 
 
-def host_link(dev, nbytes: int = 1 << 30, reps: int = 5) -> dict:
+def host_link(dev, nbytes: int = 1 << 30, reps: int = 5, mix: tuple[int, int] | None = None) -> dict:
     """Copy-engine bandwidth between pinned host memory and the device:
     host->device, device->host, and both directions at once on two streams
-    (best of `reps` copies of `nbytes`, CUDA events)."""
+    (best of `reps` copies of `nbytes`, CUDA events).  `mix` = (bytes in,
+    bytes out): also one copy of each size at once, the two directions of a
+    step's transfers alone (`step_mix_GB_s`, their total over the time)."""
     h_in = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     h_out = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     d_a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
@@ -522,15 +587,29 @@ def host_link(dev, nbytes: int = 1 << 30, reps: int = 5) -> dict:
            "how": f"cudaMemcpyAsync of {nbytes >> 20} MiB between pinned host memory and the "
                   f"device, best of {reps}; bidirectional: one copy each way on two streams"}
     del h_in, h_out, d_a, d_b
+    if mix is not None:
+        n_in, n_out = mix
+        h_in = torch.empty(n_in, dtype=torch.uint8, pin_memory=True)
+        h_out = torch.empty(n_out, dtype=torch.uint8, pin_memory=True)
+        d_a = torch.empty(n_in, dtype=torch.uint8, device=dev)
+        d_b = torch.empty(n_out, dtype=torch.uint8, device=dev)
+        out["step_mix_GB_s"] = round(gbs(best(both), n_in + n_out), 1)
+        out["how"] += (f"; step_mix: {n_in} bytes in and {n_out} bytes out at once, the copies "
+                       "of one step without the op")
+        del h_in, h_out, d_a, d_b
     return out
 
 
 def link_ceiling(bytes_step: int, h2d: int, d2h: int, link: dict) -> float:
     """The end-to-end value the host link alone allows: a step's copies in
-    and out overlapped at the measured one-way and two-way rates."""
+    and out overlapped at the measured one-way and two-way rates, and, where
+    measured, at the rate of the step's own two copies running at once
+    (each direction is slower while the other runs, so an uneven mix cannot
+    use the whole two-way rate)."""
     t_one = max(h2d / (link["h2d_GB_s"] * 1e9), d2h / (link["d2h_GB_s"] * 1e9))
     t_two = (h2d + d2h) / (link["bidirectional_GB_s"] * 1e9)
-    return bytes_step / max(t_one, t_two) / 1e9
+    t_mix = (h2d + d2h) / (link["step_mix_GB_s"] * 1e9) if "step_mix_GB_s" in link else 0.0
+    return bytes_step / max(t_one, t_two, t_mix) / 1e9
 
 
 def cpu_model() -> str:
@@ -632,27 +711,35 @@ def run_gnq(args, rank: int, world: int, barrier):
         # end to end through the public API with host buffers
         del case, g_warm, g_timed
         torch.cuda.empty_cache()
-        e2e_steps = max(1, min(args.steps, 500, int(8e9 // bytes_step)))
+        e2e_steps = max(1, min(args.steps, 500, int(16e9 // bytes_step)))
+        chunks = 4
         zc_ms, h2d, d2h = e2e_zero_copy(gnq, wl, dev, e2e_steps, 3, l2, barrier)
-        cp_ms, _, _ = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier, graph=True)
-        eager_ms, _, _ = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier, graph=False)
+        cp_runs = []
+        cp_ms, _, _ = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier, graph=True, chunks=chunks,
+                                  times=cp_runs)
+        eager_ms, _, _ = e2e_measure(gnq, wl, dev, e2e_steps, 3, barrier, graph=False,
+                                     chunks=chunks)
         gbs = lambda t: bytes_step * e2e_steps * world / (max_over_ranks(t, world, dev) / 1e3) / 1e9
-        link = host_link(dev)
+        link = host_link(dev, mix=(h2d, d2h))
         vals = {"direct": gbs(zc_ms), "copy_engine": gbs(cp_ms), "eager": gbs(eager_ms)}
         e2e = {"value": round(vals["copy_engine"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps, "row_blocks": chunks,
+               "runs_ms": [round(t, 3) for t in cp_runs],
                "direct_value": round(vals["direct"], 2),
                "eager_value": round(vals["eager"], 2),
                "host_link": link,
                "link_ceiling_value": round(link_ceiling(bytes_step, h2d, d2h, link) * world, 2),
                "how": "every step's inputs come from pinned host memory and its results go back "
-                      "to pinned host memory, through the Python API. value: explicit copies in "
-                      "and out on two streams around each call, the steps replayed from a CUDA "
-                      "graph. eager_value: the same issued one call at a time from Python. "
-                      "direct_value: the kernels read and write the host buffers over the host "
-                      "link themselves (no separate copy), graph-replayed. "
+                      "to pinned host memory, through the Python API. value: each step's rows in "
+                      f"{chunks} blocks, every block copied in on one stream, run through the op "
+                      "on a second and copied back on a third, so copies in, the op and copies "
+                      "out overlap across blocks and steps; the steps replayed from a CUDA graph, "
+                      "median of three timed runs (runs_ms). eager_value: the same issued from "
+                      "Python call by call. direct_value: the kernels read and write the host "
+                      "buffers over the host link themselves (no separate copy), graph-replayed. "
                       "link_ceiling_value: the value the measured copy-engine rates of the host "
-                      "link allow for this step's bytes in and out."}
+                      "link allow for this step's bytes in and out (host_link.step_mix_GB_s: "
+                      "the step's two copies alone, at once)."}
 
     if rank != 0:
         return None

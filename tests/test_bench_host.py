@@ -86,6 +86,23 @@ def test_link_ceiling():
     assert abs(bench.link_ceiling(10 ** 9, 4 * 10 ** 8, 10 ** 8, link) - 1000.0) < 1e-6
     link["bidirectional_GB_s"] = 250.0   # the two directions share the link: 2 ms
     assert abs(bench.link_ceiling(10 ** 9, 4 * 10 ** 8, 10 ** 8, link) - 500.0) < 1e-6
+    link["step_mix_GB_s"] = 200.0        # the step's own two copies at once: 2.5 ms
+    assert abs(bench.link_ceiling(10 ** 9, 4 * 10 ** 8, 10 ** 8, link) - 400.0) < 1e-6
+    link["step_mix_GB_s"] = 1000.0       # faster than the other bounds: they decide
+    assert abs(bench.link_ceiling(10 ** 9, 4 * 10 ** 8, 10 ** 8, link) - 500.0) < 1e-6
+
+
+@pytest.mark.parametrize("M,chunks", [(16384, 8), (16384, 1), (1000, 8), (4096, 3), (129, 2),
+                                      (100, 8), (1, 4), (128 * 5, 4)])
+def test_row_blocks_cover_the_rows_at_tile_starts(M, chunks):
+    blocks = bench.row_blocks(M, chunks)
+    assert 1 <= len(blocks) <= chunks
+    assert blocks[0][0] == 0 and blocks[-1][1] == M
+    for (a, e), (a2, _) in zip(blocks, blocks[1:]):
+        assert e == a2 and a < e
+    assert all(a % 128 == 0 for a, _ in blocks)
+    # as even as 128-row tiles allow: every block but the last is equal
+    assert len({e - a for a, e in blocks[:-1]}) <= 1
 
 
 def test_small_batch_sweep_bases():
