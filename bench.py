@@ -743,7 +743,8 @@ def run_gnq(args, rank: int, world: int, barrier):
 
     if rank != 0:
         return None
-    traffic = recorded_traffic(wl.name)
+    # the recorded traffic is the automatic launch's; a forced shape has none
+    traffic = recorded_traffic(wl.name) if args.policy == "0,0,0,0" else None
     line = {
         "metric": METRIC,
         "value": round(value, 2),
