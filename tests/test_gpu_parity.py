@@ -595,33 +595,48 @@ def test_binding_rejects_bad_buffers(gnq):
                                            out=(q, None, None))              # q sized for NVFP4
 
 
-def test_bounded_wait_gives_up_and_the_next_call_is_clean(gnq):
+@pytest.mark.parametrize("mode,scale,vpt,form,residual", [
+    ("fp8", 0.05, 0, 0, False),
+    # the packed NVFP4 form agrees on the copies' arrival at its row barrier
+    # and stores the new residual after it
+    ("nvfp4", 168.0, 4, 2, False),
+    ("nvfp4", 168.0, 4, 2, True),
+    ("nvfp4", 168.0, 2, 1, True),
+])
+def test_bounded_wait_gives_up_and_the_next_call_is_clean(gnq, mode, scale, vpt, form, residual):
     """The failure path of the streaming kernel's bounded waits, on the GPU
     without a fault: under the library's test hook every row announces 16
     bytes more than its copies deliver, so no barrier can complete and each
     CTA's first wait runs out (after ~2^20 cycles).  The kernel must set the
     timeout bit of the device error word, complete its barriers itself with
-    one more valid copy, and return without writing any output; the next
-    normal call must then pass the whole parity contract."""
+    one more valid copy, and return without writing any output (codes,
+    scales, y, the residual); the next normal call must then pass the whole
+    parity contract."""
     dev = torch.device("cuda")
     M, H = 700, 2048
-    x, _, w = _make(M, H, "bf16", seed=61, residual=False)
+    x, r, w = _make(M, H, "bf16", seed=61, residual=residual)
     xd, wd = x.to(dev), w.to(dev)
-    sd = torch.tensor([0.05], device=dev)
+    rd = None if r is None else r.to(dev)
+    sd = torch.tensor([scale], device=dev)
     assert gnq.read_device_error(clear=True) == 0
-    q, _, _ = gnq.alloc_outputs(M, H, "fp8", False, xd)
-    q.view(torch.uint8).fill_(0xA5)
-    with forced_policy(gnq, 2):
+    q, bs, y = gnq.alloc_outputs(M, H, mode, True, xd)
+    for t in (q, bs, y):
+        if t is not None:
+            t.view(torch.uint8).fill_(0xA5)
+    with forced_policy(gnq, 2, 0, vpt, form):
         gnq.inject_wait_timeout(True)
         try:
-            gnq.gemma_add_rms_norm_quant(xd, None, wd, 1e-6, sd, "fp8", write_y=False,
-                                         out=(q, None, None))
+            gnq.gemma_add_rms_norm_quant(xd, rd, wd, 1e-6, sd, mode, write_y=True, out=(q, bs, y))
             torch.cuda.synchronize()
         finally:
             gnq.inject_wait_timeout(False)
         assert gnq.read_device_error(clear=True) & 1, "the timeout bit was not set"
-        assert bool((q.view(torch.uint8) == 0xA5).all()), "a timed-out call wrote codes"
-        run_case(gnq, x, None, w, "fp8", 0.05, write_y=False, dtype="bf16")
+        for name, t in (("codes", q), ("scales", bs), ("y", y)):
+            if t is not None:
+                assert bool((t.view(torch.uint8) == 0xA5).all()), f"a timed-out call wrote {name}"
+        if r is not None:
+            assert torch.equal(rd.cpu(), r), "a timed-out call wrote the residual"
+        run_case(gnq, x, r, w, mode, scale, write_y=True, dtype="bf16")
     assert gnq.read_device_error() == 0
 
 
