@@ -526,7 +526,15 @@ __device__ __forceinline__ float div6(float amax) {
 // Wait until the grid this one depends on has completed and its memory is
 // visible (returns at once when the launch was not programmatic).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Allow the dependent grid to begin launching.
+// Allow the dependent grid to begin launching.  Every grid triggers right
+// after its wait, at every batch size: the dependent launches only once all
+// of this grid's CTAs have started, so it can only take SMs this grid has
+// released.  With a stand-in next-layer kernel as the dependent (the bench's
+// PDL consumer sweep, M = 1..8192 at H = 5120) the early trigger led plain
+// launches and a trigger at exit at every M in FP8 and NVFP4, including
+// M >= 192, where "vllm.models.qwen3_5.nvidia.ops.fused_norm_quant"
+// (gemma_add_rms_norm_quant, TRIGGER_EARLY) turns its early trigger off
+// because the prelaunched next linear took SMs.
 __device__ __forceinline__ void pdl_trigger() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

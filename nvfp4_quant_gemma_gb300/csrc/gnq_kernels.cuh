@@ -556,6 +556,7 @@ __global__ void __launch_bounds__(1024 / VPT) __maxnreg__((RowForm<MODE, VPT, PA
 // NVFP4, not LEAN, several units per thread: bias + w lives in shared
 // memory (chunk j of unit u at float4 index j * H/E + u, so a warp's reads
 // are conflict-free), which frees the registers for a third resident CTA.
+
 // Thread 0 of a streaming CTA whose wait for local row i (stage s, phase
 // parity) gave up: set the error bit and wait, bounded, for every copy still
 // in flight (rows i .. i + S - 1) before the CTA's shared memory goes away.
