@@ -40,11 +40,17 @@ MUTATIONS = [
      "or_e4m3_encode((double)yf[32 * b + j])"),
     ("swizzle_tile_row_stride", "(m / 128) * (Kp / 4) + k / 4", "(m / 128) * Kp + k / 4"),
     ("swizzle_tile_col_stride", "(m / 128) * (Kp / 4) + k / 4", "(m / 128) * (Kp / 4) + k / 2"),
+    ("no_square_root", "1.0 / sqrt(ss / (double)H + (double)eps)", "1.0 / (ss / (double)H + (double)eps)"),
 ]
 
+# Slips the symmetry pins (tests/test_oracle_symmetries.py) must catch on
+# their own, without the hand-worked examples.
+SYMMETRY_MUTATIONS = [m for m in MUTATIONS
+                      if m[0] in ("drop_eps", "residual_not_used", "e2m1_no_saturation_sign",
+                                  "no_square_root")]
 
-@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
-def test_pins_catch_planted_slip(tmp_path, name, old, new):
+
+def _fails_with(tmp_path, name, old, new, pins):
     src = open(SRC).read()
     assert src.count(old) == 1, f"mutation anchor for {name} not unique"
     mutated = tmp_path / "oracle.c"
@@ -55,5 +61,17 @@ def test_pins_catch_planted_slip(tmp_path, name, old, new):
                     str(mutated), "-o", str(lib), "-lm"], check=True)
     env = dict(os.environ, GNQ_ORACLE_LIB=str(lib))
     res = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                          *PINS], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert res.returncode != 0, f"pins did not catch the planted slip {name}"
+                          *pins], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    # exit status 1: tests ran and one failed (not a collection or usage error)
+    assert res.returncode == 1, (f"pins did not catch the planted slip {name} "
+                                 f"(pytest status {res.returncode}):\n{res.stdout[-2000:]}")
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pins_catch_planted_slip(tmp_path, name, old, new):
+    _fails_with(tmp_path, name, old, new, PINS)
+
+
+@pytest.mark.parametrize("name,old,new", SYMMETRY_MUTATIONS, ids=[m[0] for m in SYMMETRY_MUTATIONS])
+def test_symmetry_pins_alone_catch_planted_slip(tmp_path, name, old, new):
+    _fails_with(tmp_path, name, old, new, ["tests/test_oracle_symmetries.py"])
