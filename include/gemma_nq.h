@@ -210,7 +210,13 @@ int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y,
  * Programmatic dependent launch (on by default): each launch may start while
  * the preceding kernel on the stream drains, and waits inside the kernel
  * (griddepcontrol.wait) until that kernel's results are visible before its
- * first global read; right after that wait it also lets a programmatic
+ * first global read of them.  Before the wait, the CTAs that can be waiting
+ * (the first wave of a one-CTA-per-row launch; the NVFP4 streaming CTAs for
+ * their first rows) prefetch their rows of x, the partials and the residual
+ * into L2: a cache hint, not a read (the values used are loaded after the
+ * wait, and L2 is where the preceding kernel's stores land), so the
+ * buffers must be valid device-accessible memory at launch, as for any
+ * call.  Right after the wait the kernel also lets a programmatic
  * dependent that follows it launch (that kernel must wait in the same way
  * before reading these outputs), so the dependent's CTAs can take the SMs
  * this grid leaves idle and run their own prologue early.  Results are

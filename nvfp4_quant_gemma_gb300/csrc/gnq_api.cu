@@ -99,6 +99,35 @@ cudaError_t opt_in_dynamic_smem(const void *fn) {
     return e;
 }
 
+int one_wave_ctas(const void *fn, int threads) {
+    struct Entry {
+        int dev;
+        const void *fn;
+        int threads, ctas;
+    };
+    static std::mutex mu;
+    static Entry cache[512];
+    static int n_cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_cached; ++i)
+            if (cache[i].dev == dev && cache[i].fn == fn && cache[i].threads == threads)
+                return cache[i].ctas;
+    }
+    int per_sm = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, 0) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int ctas = per_sm * sms;
+    std::lock_guard<std::mutex> lock(mu);
+    if (n_cached < 512) cache[n_cached++] = Entry{dev, fn, threads, ctas};
+    return ctas;
+}
+
 namespace {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -372,6 +401,7 @@ int run(const void *x, int k, int64_t part_stride, void *residual, const void *w
     const bool inject = g_inject_timeout.load() != 0;
     p.wait_limit = inject ? kTestWaitLimit : kWaitLimit;
     p.tx_extra = inject ? 16u : 0u;
+    p.pf_ctas = 0;  // set per launch
 
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool parts = k > 1;

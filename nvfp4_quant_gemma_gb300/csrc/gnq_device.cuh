@@ -46,6 +46,7 @@ struct Params {
     unsigned int *err;    // device error word
     long long wait_limit; // clock cycles a bounded wait may spin
     uint32_t tx_extra;    // test hook: bytes announced per row beyond the copies (0 or 16)
+    int pf_ctas;          // row kernel: CTAs below this index prefetch their rows before the wait
 };
 
 // ---------------------------------------------------------------------------
@@ -619,6 +620,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
         : "memory");
+}
+// Cache hints: bring global memory into L2 (no value is read, no effect on
+// what a later load returns; L2 is where every SM's accesses meet).
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void fence_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -35,6 +35,11 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
 // gnq_api.cu.)
 cudaError_t opt_in_dynamic_smem(const void *fn);
 
+// CTAs of this instance that one wave holds on the current device (resident
+// CTAs per SM x SMs; 0 on error), cached per device, instance and block size.
+// (Defined in gnq_api.cu.)
+int one_wave_ctas(const void *fn, int threads);
+
 // Resident CTAs per SM of the streaming kernel instance for this shape (0 on
 // error); opts the instance in to its largest dynamic shared memory.
 template <int MODE>
@@ -131,6 +136,8 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
         const cudaError_t e = opt_in_dynamic_smem(reinterpret_cast<const void *>(fn));
         if (e != cudaSuccess) return e;
     }
+    Params q = p;
+    q.pf_ctas = ls.stream ? 0 : one_wave_ctas(reinterpret_cast<const void *>(fn), ls.threads);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ls.grid, 1, 1);
     cfg.blockDim = dim3((unsigned)ls.threads, 1, 1);
@@ -152,7 +159,7 @@ cudaError_t launch_mode(const Params &p, int dtype, bool parts, const LaunchShap
     }
     cfg.numAttrs = n;
     cfg.attrs = attr;
-    return cudaLaunchKernelEx(&cfg, fn, p);
+    return cudaLaunchKernelEx(&cfg, fn, q);
 }
 
 }  // namespace gnq
