@@ -592,6 +592,18 @@ __device__ __forceinline__ void stream_drain(const Params &p, int i, int n_rows,
     }
 }
 
+// Thread 0 of a streaming CTA: its first n rows (m = b, b + G, ...) into L2
+// before the wait.  Not inlined, so that the hot loop of the instances that
+// call it keeps its own code.
+static __device__ __noinline__ void stream_prefetch_rows(const Params &p, int64_t b, int G, int n,
+                                                         uint32_t row_bytes) {
+    for (int i = 0; i < n; ++i) {
+        const int64_t m = b + (int64_t)i * G;
+        for (int op = 0; op < p.k; ++op) prefetch_l2_bulk(p.x + op * p.part_stride + m * p.H, row_bytes);
+        if (p.residual) prefetch_l2_bulk(p.residual + m * p.H, row_bytes);
+    }
+}
+
 // maxnreg: the register budget of the NVFP4 instances (stream_kernel_nvfp4):
 // 80 for the shared-memory-weight form at two units per thread (three
 // resident CTAs of 256 threads), else what the launch bound allows.
@@ -640,9 +652,17 @@ __device__ __forceinline__ void stream_body(const Params &p, uint8_t *dsmem, flo
         if (p.residual) bulk_g2s(dst + row_bytes * p.k, p.residual + m * p.H, row_bytes, bar);
     };
 
-    // NVFP4: the first rows' inputs into L2 while the preceding grid drains
-    // (a hint; fp16 16384 x 8192 without residual 55.42 -> 53.69 us, k = 4
-    // partials 64.07 -> 62.43 us; FP8 lost 3.7 % with it).
+    // The first rows' inputs into L2 while the preceding grid drains (a
+    // hint).  NVFP4, inlined: fp16 16384 x 8192 without residual 55.42 ->
+    // 53.69 us, k = 4 partials 64.07 -> 62.43 us.  The FP8 family through
+    // the helper, where it measured faster: bf16 FP8 16384 x 8192 without
+    // residual 70.3 -> 63.0 us (4096 rows 21.6 -> 17.5), fp16 MXFP8 67.5 ->
+    // 65.0; the fp16 FP8 instances keep their code (with the call compiled
+    // in, 62.5 -> 63.2 us, and 65.1 with it skipped at run time).
+    if constexpr (MODE != MODE_NVFP4 &&
+                  (MODE == MODE_MXFP8 || std::is_same<T, __nv_bfloat16>::value)) {
+        if (t == 0) stream_prefetch_rows(p, blockIdx.x, G, n_rows < S ? n_rows : S, row_bytes);
+    }
     if (MODE == MODE_NVFP4 && t == 0) {
         for (int i = 0; i < n_rows && i < S; ++i) {
             const int64_t m = blockIdx.x + (int64_t)i * G;
