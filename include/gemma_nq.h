@@ -211,8 +211,9 @@ int gnq_query_launch(int64_t M, int64_t H, int k, int has_residual, int write_y,
  * the preceding kernel on the stream drains, and waits inside the kernel
  * (griddepcontrol.wait) until that kernel's results are visible before its
  * first global read of them.  Before the wait, the CTAs that can be waiting
- * (the first wave of a one-CTA-per-row launch; the NVFP4 streaming CTAs for
- * their first rows) prefetch their rows of x, the partials and the residual
+ * (the first wave of a one-CTA-per-row launch; streaming CTAs, for their
+ * first rows, in the NVFP4, MXFP8 and bf16 instances) prefetch their rows
+ * of x, the partials and the residual
  * into L2: a cache hint, not a read (the values used are loaded after the
  * wait, and L2 is where the preceding kernel's stores land), so the
  * buffers must be valid device-accessible memory at launch, as for any
