@@ -496,6 +496,57 @@ def test_pdl_on_and_off_agree(gnq, mode, scale, M, k):
         assert all(torch.equal(a, b) for a, b in zip(ref, got))
 
 
+@pytest.mark.parametrize("mode,scale", [("fp8", 0.05), ("nvfp4", 168.0), ("mxfp8", 0.0)])
+@pytest.mark.parametrize("M", [64, 2048])
+def test_pdl_chain_whose_x_is_the_previous_y(gnq, mode, scale, M):
+    """A chain in which every call's activation x is the y the previous call
+    wrote (and its residual the residual it updated), as when the producing
+    kernel writes x: the rows each call prefetches before its wait are still
+    being written by its predecessor.  PDL on (eagerly and in a captured
+    graph) gives the bits of plain launches, in one-wave and many-wave
+    grids."""
+    dev = torch.device("cuda")
+    H = 4096
+    x, r, w = _make(M, H, "bf16", seed=37)
+    wd = w.to(dev)
+    sd = torch.tensor([scale], device=dev)
+
+    def chain(pdl, graph):
+        gnq.set_pdl(pdl)
+        try:
+            rd = r.to(dev)
+            x0 = x.to(dev)
+            outs = [gnq.alloc_outputs(M, H, mode, True, x0) for _ in range(4)]
+            for o in outs:  # NVFP4 scale padding rows are never written
+                if o[1] is not None:
+                    o[1].view(torch.uint8).fill_(0xA5)
+            def run():
+                xi = x0
+                for o in outs:
+                    gnq.gemma_add_rms_norm_quant(xi, rd, wd, 1e-6, sd, mode, write_y=True, out=o)
+                    xi = o[2]  # the next call normalizes this call's y
+            if graph:
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    run()
+                rd.copy_(r.to(dev))
+                for o in outs:
+                    o[2].zero_()
+                g.replay()
+            else:
+                run()
+            torch.cuda.synchronize()
+            return [rd.clone()] + [t.view(torch.uint8).clone() for o in outs for t in o if t is not None]
+        finally:
+            gnq.set_pdl(True)
+
+    ref = chain(False, False)
+    for pdl, graph in ((True, False), (True, True)):
+        got = chain(pdl, graph)
+        assert all(torch.equal(a, b) for a, b in zip(ref, got))
+    assert gnq.read_device_error() == 0
+
+
 def test_status_codes_with_device_buffers(gnq):
     lib = gnq.load()
     import ctypes
