@@ -623,8 +623,10 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 // Cache hints: bring global memory into L2 (no value is read, no effect on
 // what a later load returns; L2 is where every SM's accesses meet).
-__device__ __forceinline__ void prefetch_l2_line(const void *p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+// `last`: with the evict-last priority, kept in L2 ahead of other lines.
+__device__ __forceinline__ void prefetch_l2_line(const void *p, bool last) {
+    if (last) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+    else asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 __device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
